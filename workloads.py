@@ -1,0 +1,138 @@
+"""Seeded synthetic inputs for packed variable-length attention.
+
+This module is shared by the CPU oracle's tests and by the CUDA path's tests
+and benchmark.  It holds no attention arithmetic: it only draws random
+numbers, rounds them to the bf16 input type and builds the ``cu_seqlens``
+prefix sums.
+
+What it follows (atrex-bench "attention_forward", page #001, ``input.py``):
+q, k and v are drawn i.i.d. N(0, 1) in bf16 with shape
+``[total_tokens, num_heads, head_dim]`` and ``cu_seqlens_q = cu_seqlens_k`` is
+the prefix sum of the per-sequence lengths.  The page draws unseeded on the
+GPU; here every draw is seeded on the host so both sides see identical bits:
+``numpy.random.default_rng(seed).standard_normal(..., dtype=float32)`` in the
+order q, k, v, each rounded to bf16 by round-to-nearest-even on the bit
+pattern.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One attention call: sequence lengths, heads and head size."""
+
+    name: str
+    seq_lens_q: tuple
+    num_heads: int
+    head_dim: int
+    seed: int
+    seq_lens_k: tuple | None = None   # None: same as seq_lens_q
+    cu_offset: int = 0                # rows before the first sequence
+    description: str = ""
+
+    @property
+    def lens_k(self) -> tuple:
+        return self.seq_lens_q if self.seq_lens_k is None else self.seq_lens_k
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.seq_lens_q)
+
+    def cu_seqlens(self):
+        """int32 prefix sums (q, k), each of length num_seqs + 1."""
+        cu_q = np.zeros(self.num_seqs + 1, dtype=np.int64)
+        cu_k = np.zeros(self.num_seqs + 1, dtype=np.int64)
+        cu_q[0] = cu_k[0] = self.cu_offset
+        cu_q[1:] = self.cu_offset + np.cumsum(self.seq_lens_q)
+        cu_k[1:] = self.cu_offset + np.cumsum(self.lens_k)
+        return cu_q.astype(np.int32), cu_k.astype(np.int32)
+
+    @property
+    def total_q(self) -> int:
+        return int(self.cu_offset + sum(self.seq_lens_q))
+
+    @property
+    def total_k(self) -> int:
+        return int(self.cu_offset + sum(self.lens_k))
+
+    def flops(self) -> float:
+        """The metric's FLOP count 4 * sum(L_q * L_k) * H * D (true head_dim)."""
+        s = sum(int(a) * int(b) for a, b in zip(self.seq_lens_q, self.lens_k)
+                if a > 0 and b > 0)
+        return 4.0 * s * self.num_heads * self.head_dim
+
+    def algorithmic_bytes(self) -> int:
+        """bf16 bytes of q, k, v read once and out written once."""
+        rows_q = sum(max(int(a), 0) for a in self.seq_lens_q)
+        rows_k = sum(max(int(b), 0) for a, b in zip(self.seq_lens_q, self.lens_k)
+                     if a > 0)
+        row = self.num_heads * self.head_dim * 2
+        return (2 * rows_q + 2 * rows_k) * row
+
+
+# The five workloads: four rows of the page's shape table (#4, #8, #9, #11)
+# and one packed batch made of rows #11-#17 plus a length-1 and an empty
+# sequence.
+C1 = Workload("C1_L276_H4_D72", (276,), 4, 72, seed=1,
+              description="one sequence L=276, H=4, D=72 (shape-table row #11)")
+C2 = Workload("C2_L8136_H16_D72", (8136,), 16, 72, seed=2,
+              description="one sequence L=8136, H=16, D=72 (shape-table row #4)")
+C3 = Workload("C3_L16742_H32_D128", (16742,), 32, 128, seed=3,
+              description="one sequence L=16742, H=32, D=128 (shape-table row #9)")
+C4 = Workload("C4_L65556_H16_D72", (65556,), 16, 72, seed=4,
+              description="one sequence L=65556, H=16, D=72 (shape-table row #8)")
+C5 = Workload("C5_packed9_T31673_H4_D72",
+              (1, 276, 600, 1012, 2024, 4100, 8184, 15476, 0), 4, 72, seed=5,
+              description="packed batch of 9 sequences (rows #11-#17, a length-1 "
+                          "and an empty one), T=31673, H=4, D=72")
+
+CONFIGS = {"C1": C1, "C2": C2, "C3": C3, "C4": C4, "C5": C5}
+
+
+def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns (uint16), round to nearest, ties to even."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = u + 0x7FFF + ((u >> 16) & 1)
+    return (u >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> exact float64 values."""
+    u = np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def make_inputs(w: Workload):
+    """Return dict with q, k, v (uint16 bf16 bits, [T, H, D]) and cu_q, cu_k (int32)."""
+    rng = np.random.default_rng(w.seed)
+    H, D = w.num_heads, w.head_dim
+    q = round_to_bf16_bits(rng.standard_normal((w.total_q, H, D), dtype=np.float32))
+    k = round_to_bf16_bits(rng.standard_normal((w.total_k, H, D), dtype=np.float32))
+    v = round_to_bf16_bits(rng.standard_normal((w.total_k, H, D), dtype=np.float32))
+    cu_q, cu_k = w.cu_seqlens()
+    return {"q": q, "k": k, "v": v, "cu_q": cu_q, "cu_k": cu_k}
+
+
+def sample_rows(w: Workload, rows_per_head: int, seed_offset: int = 1000):
+    """Seeded subset of (token, head) output rows, drawn independently per head.
+
+    Only tokens that belong to a non-empty query sequence are drawn.  Returns
+    an int64 array of shape [n, 2] with columns (token index, head).
+    """
+    rng = np.random.default_rng(w.seed + seed_offset)
+    cu_q, _ = w.cu_seqlens()
+    covered = []
+    for i in range(w.num_seqs):
+        if cu_q[i + 1] > cu_q[i]:
+            covered.append(np.arange(cu_q[i], cu_q[i + 1]))
+    tokens = np.concatenate(covered) if covered else np.zeros(0, dtype=np.int64)
+    out = []
+    for h in range(w.num_heads):
+        n = min(rows_per_head, tokens.size)
+        pick = np.sort(rng.choice(tokens.size, size=n, replace=False))
+        out.append(np.stack([tokens[pick], np.full(n, h)], axis=1))
+    return np.concatenate(out).astype(np.int64)
