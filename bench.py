@@ -1,0 +1,321 @@
+#!/usr/bin/env python3
+"""Benchmark of the packed variable-length attention forward on one GB300.
+
+One step = one call of the whole path (plan kernel + fused attention kernel)
+over one batch of synthetic input resident in HBM.  The headline workload is
+one sequence L=8136, 16 heads, head_dim 72 (attention_forward shape-table
+row #4); the line also carries every workload's microseconds and TFLOP/s
+under "shapes".  Metric: TFLOP/s with FLOPs = 4 * sum(L_q * L_k) * H * D
+(true head_dim).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (weak
+scaling, no collective on the data path); rank 0 prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads import C1, C2, C3, C4, C5, make_inputs, sample_rows  # noqa: E402
+
+HEADLINE = C2
+METRIC = "varlen attn fwd TFLOP/s (4*sum(L^2)*H*D)"
+PAGE_TPROD_TFLOPS = {  # the page's T_Prod converted with the same FLOP count
+    C1.name: 2.0, C2.name: 80.5, C3.name: 123.1, C4.name: 83.3}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_tflops": d["bf16_tflops"], "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm, smax = float(parts[1]), float(parts[2])
+                except ValueError:
+                    continue
+                sms.append(sm)
+                mx = smax
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        busy = [s for s in sms if mx and s > 0.3 * mx] or sms
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def cpu_oracle_rate(w, max_seconds=12.0, nthreads=0):
+    """Oracle throughput on a bounded, seeded sample of rows of workload w."""
+    import oracle
+    x = make_inputs(w)
+    rows_all = sample_rows(w, 4096, seed_offset=2000)
+    cu = x["cu_q"]
+    # rows of one head, all keys of their sequence: time a growing sample
+    n = 64
+    t_used, done_rows, done_flops = 0.0, 0, 0.0
+    lk = np.diff(x["cu_k"])
+    seq_of = np.searchsorted(cu, rows_all[:, 0], side="right") - 1
+    start = 0
+    while t_used < max_seconds and start < rows_all.shape[0]:
+        rows = rows_all[start:start + n]
+        t0 = time.perf_counter()
+        oracle.attn_rows(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], rows, nthreads=nthreads)
+        t_used += time.perf_counter() - t0
+        done_rows += rows.shape[0]
+        done_flops += float(np.sum(4.0 * lk[seq_of[start:start + n]] * w.head_dim))
+        start += n
+        n = min(n * 2, 4096)
+    return {"rows": done_rows, "seconds": t_used, "tflops": done_flops / t_used / 1e12,
+            "rows_per_s": done_rows / t_used, "cores": oracle.max_threads(nthreads)}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, timed on the host cores."""
+    if rank != 0:
+        return
+    w = HEADLINE
+    r = cpu_oracle_rate(w, max_seconds=max(2.0, 20.0 / max(args.steps, 1)))
+    ms_per_step = None
+    vals = []
+    for _ in range(args.steps):
+        vals.append(cpu_oracle_rate(w, max_seconds=max(1.0, 20.0 / max(args.steps, 1)))["tflops"])
+    val = statistics.median(vals) if vals else r["tflops"]
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "seq_lens": list(w.seq_lens_q), "num_heads": w.num_heads,
+                       "head_dim": w.head_dim},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
+                             "sample": f"seeded rows of {w.name} (all keys per row), about "
+                                       f"{max(1.0, 20.0 / max(args.steps, 1)):.0f} s per step"},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def time_calls(fn, steps, flush_buf, stream):
+    import torch
+    durs = []
+    for _ in range(steps):
+        if flush_buf is not None:
+            flush_buf.fill_(1)  # write > L2 so every step reads its inputs from HBM
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        durs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in durs]
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import variable_length_prefill_gb300 as vlp
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    vlp.load()
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    def device_inputs(w):
+        x = make_inputs(w)
+        t = {n: torch.from_numpy(x[n].view(np.int16)).view(torch.bfloat16).to(dev)
+             for n in ("q", "k", "v")}
+        return x, t, torch.from_numpy(x["cu_q"]).to(dev), torch.from_numpy(x["cu_k"]).to(dev)
+
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    w = HEADLINE
+    x, t, cu_q, cu_k = device_inputs(w)
+    out = torch.empty_like(t["q"])
+    step = lambda: vlp.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, out=out)  # noqa: E731
+    for _ in range(args.warmup):
+        step()
+    vlp.check()
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        durs = time_calls(step, args.steps, flush, stream)
+    vlp.check()
+    t_sum = sum(durs) / 1e3  # seconds of device time over the K steps
+    if world > 1:
+        tt = torch.tensor([t_sum], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_sum = float(tt.item())
+    flops = w.flops()
+    value = flops * args.steps * world / t_sum / 1e12
+    ms_per_step = t_sum / args.steps * 1e3
+    per_call_tflops = flops / (t_sum / args.steps) / 1e12
+
+    # end to end through the public API with host buffers (pinned), copies included
+    host = {n: torch.from_numpy(x[n].view(np.int16)).pin_memory() for n in ("q", "k", "v")}
+    hcu_q = torch.from_numpy(x["cu_q"]).pin_memory()
+    hcu_k = torch.from_numpy(x["cu_k"]).pin_memory()
+    hout = torch.empty(host["q"].shape, dtype=torch.int16).pin_memory()
+    dq = torch.empty_like(t["q"]); dk = torch.empty_like(t["k"]); dv = torch.empty_like(t["v"])
+    dcq = torch.empty_like(cu_q); dck = torch.empty_like(cu_k)
+    h2d = sum(v.numel() * v.element_size() for v in host.values()) + 2 * hcu_q.numel() * 4
+    d2h = hout.numel() * 2
+
+    def e2e_step():
+        dq.view(torch.int16).copy_(host["q"], non_blocking=True)
+        dk.view(torch.int16).copy_(host["k"], non_blocking=True)
+        dv.view(torch.int16).copy_(host["v"], non_blocking=True)
+        dcq.copy_(hcu_q, non_blocking=True)
+        dck.copy_(hcu_k, non_blocking=True)
+        vlp.attn_varlen_fwd(dq, dk, dv, dcq, dck, out=out)
+        hout.copy_(out.view(torch.int16), non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_durs = time_calls(e2e_step, e2e_steps, None, stream)
+    e2e_value = flops / (sum(e2e_durs) / 1e3 / e2e_steps) / 1e12 * world
+
+    # every workload once more: microseconds per call and TFLOP/s
+    shapes = {}
+    if not args.headline_only:
+        for ws in (C1, C2, C3, C4, C5):
+            xs, ts, cq, ck = device_inputs(ws)
+            os_ = torch.empty_like(ts["q"])
+            fn = lambda: vlp.attn_varlen_fwd(ts["q"], ts["k"], ts["v"], cq, ck, out=os_)  # noqa: E731
+            for _ in range(3):
+                fn()
+            n = 5 if ws is C4 else 20
+            d = time_calls(fn, n, flush, stream)
+            us = statistics.median(d) * 1e3
+            tf = ws.flops() / (us * 1e-6) / 1e12
+            shapes[ws.name] = {"us": round(us, 2), "tflops": round(tf, 2),
+                               "pct_bf16_peak": round(100.0 * tf / peaks["bf16_tflops"], 2),
+                               "page_tprod_tflops": PAGE_TPROD_TFLOPS.get(ws.name)}
+            del ts, os_
+        vlp.check()
+
+    if rank != 0:
+        return
+    cpu = cpu_oracle_rate(w, max_seconds=args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": round(value / world / PAGE_TPROD_TFLOPS[w.name], 3),
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "seq_lens": list(w.seq_lens_q), "num_heads": w.num_heads,
+                   "head_dim": w.head_dim, "l2": "flushed before every step (256 MiB write)"},
+        "roofline": {"bound": "tensor", "achieved": round(per_call_tflops, 2),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(per_call_tflops / peaks["bf16_tflops"], 4),
+                     "traffic": None, "peak_source": peaks["source"] + " bf16 burst",
+                     "kernel": "attn_varlen_fwd_kernel<72> (+ plan kernel in the timed call)"},
+        "cpu_baseline": {"value": cpu["tflops"], "unit": "TFLOP/s", "cores": cpu["cores"],
+                         "kind": "oracle", "rows_per_s": cpu["rows_per_s"],
+                         "sample": f"{cpu['rows']} seeded (token, head) rows of {w.name}, "
+                                   f"all keys each, {cpu['seconds']:.1f} s"},
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+        "shapes": shapes,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

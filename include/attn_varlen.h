@@ -1,0 +1,126 @@
+/*
+ * attn_varlen.h -- C ABI of the GB300 (sm_103a) packed variable-length
+ * attention forward.
+ *
+ * The operation is atrex-bench "attention_forward" (page #001, reference.py,
+ * Model.forward): for every sequence i whose query slice
+ * [cu_seqlens_q[i], cu_seqlens_q[i+1]) is non-empty and every head h,
+ *
+ *     out[slice_q, h, :] = softmax(q[slice_q, h, :] . k[slice_k, h, :]^T * D^-1/2)
+ *                          . v[slice_k, h, :]
+ *
+ * with slice_k = [cu_seqlens_k[i], cu_seqlens_k[i+1]), non-causal, and the
+ * scale fixed at head_dim^-1/2 (the page passes no scale, so the library
+ * default applies, computed with the true head_dim).  Sequences with an empty
+ * query slice are skipped (the page's loop does the same); a non-empty query
+ * slice with an empty key slice gets zero rows.  Output rows that no query
+ * slice covers are never written (the page allocates the output with
+ * empty_like).
+ *
+ * Layout (page #001, input.py): q, out are bf16 [total_q, num_heads,
+ * head_dim] and k, v are bf16 [total_k, num_heads, head_dim], contiguous,
+ * token-major; cu_seqlens_q/k are int32 [num_seqs + 1] prefix offsets in
+ * DEVICE memory.  Every pointer argument below is a caller-owned CUDA device
+ * pointer that the library never frees.  Calls are asynchronous on `stream`:
+ * the library never copies cu_seqlens to the host and never synchronises,
+ * except when it grows its own workspace (see attn_varlen_fwd).
+ *
+ * Preconditions the library cannot check without reading device memory:
+ * every offset in cu_seqlens_q lies in [0, total_q] and every offset in
+ * cu_seqlens_k in [0, total_k], where total_* is the row count of the
+ * caller's buffers.  A negative slice length is read as an empty slice.
+ */
+#ifndef ATTN_VARLEN_H
+#define ATTN_VARLEN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define ATTN_VARLEN_OK                     0
+#define ATTN_VARLEN_ERR_INVALID_ARG       -1  /* null pointer, negative count, ... */
+#define ATTN_VARLEN_ERR_UNSUPPORTED_DIM   -2  /* head_dim not 72 or 128            */
+#define ATTN_VARLEN_ERR_MISALIGNED        -3  /* q, k, v or out not 16-byte aligned */
+#define ATTN_VARLEN_ERR_UNSUPPORTED_DEVICE -4 /* current device is not sm_103       */
+#define ATTN_VARLEN_ERR_CUDA              -5  /* a CUDA runtime call failed         */
+#define ATTN_VARLEN_ERR_OOM               -6  /* workspace allocation failed        */
+#define ATTN_VARLEN_ERR_DEVICE_TIMEOUT    -7  /* a kernel wait ran out of time      */
+#define ATTN_VARLEN_ERR_WORKSPACE_SMALL   -8  /* caller workspace below the minimum */
+#define ATTN_VARLEN_ERR_DRIVER            -9  /* tensor-map encoder unavailable     */
+
+/*
+ * attn_varlen_fwd -- the attention forward described above.
+ *
+ *   q, k, v       bf16 device buffers, layout above, 16-byte aligned
+ *   cu_seqlens_q  int32 device array [num_seqs + 1]
+ *   cu_seqlens_k  int32 device array [num_seqs + 1]
+ *   num_seqs      >= 0; 0 returns ATTN_VARLEN_OK without launching anything
+ *   num_heads     >= 1 (query, key and value heads are the same count)
+ *   head_dim      72 or 128
+ *   out           bf16 device buffer [total_q, num_heads, head_dim], 16-byte
+ *                 aligned; must not overlap q, k or v
+ *   stream        CUDA stream the work is queued on (0 = legacy default)
+ *
+ * Uses a workspace that the library owns, one per device, sized by num_seqs.
+ * When it must grow, the call synchronises the device once to free the old
+ * one.  Calls that share a device must be ordered (same stream, or
+ * synchronised); concurrent calls on different streams must each pass their
+ * own workspace to attn_varlen_fwd_ws.  Errors detected inside the kernels
+ * (a wait that timed out) are recorded in the workspace and reported by
+ * attn_varlen_check.  Returns an ATTN_VARLEN_* code.
+ */
+int attn_varlen_fwd(const void* q, const void* k, const void* v,
+                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                    int num_seqs, int num_heads, int head_dim,
+                    void* out, cudaStream_t stream);
+
+/* Bytes of workspace attn_varlen_fwd_ws needs for num_seqs sequences
+ * (0 for num_seqs < 0). */
+size_t attn_varlen_workspace_size(int num_seqs);
+
+/*
+ * attn_varlen_fwd_ws -- attn_varlen_fwd with a caller-owned workspace.
+ *
+ *   workspace        device buffer, 256-byte aligned, at least
+ *                    attn_varlen_workspace_size(num_seqs) bytes, zero-filled
+ *                    before its first use (the first 4 bytes are the sticky
+ *                    device status word; the rest is rewritten every call)
+ *   workspace_bytes  its size in bytes
+ *
+ * Calls that share one workspace must be ordered on the device.  Nothing is
+ * allocated.  Returns an ATTN_VARLEN_* code.
+ */
+int attn_varlen_fwd_ws(const void* q, const void* k, const void* v,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                       int num_seqs, int num_heads, int head_dim, void* out,
+                       void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/*
+ * attn_varlen_check -- synchronise `stream`, then read and clear the status
+ * word of the current device's library-owned workspace.  Returns
+ * ATTN_VARLEN_OK, ATTN_VARLEN_ERR_DEVICE_TIMEOUT when a kernel wait ran out of
+ * time since the last check, or ATTN_VARLEN_ERR_CUDA when the stream reports
+ * an error.
+ */
+int attn_varlen_check(cudaStream_t stream);
+
+/* attn_varlen_check for a caller-owned workspace. */
+int attn_varlen_check_ws(void* workspace, cudaStream_t stream);
+
+/* Static, human-readable text for an ATTN_VARLEN_* code. */
+const char* attn_varlen_strerror(int code);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int attn_varlen_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_VARLEN_H */

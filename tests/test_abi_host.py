@@ -1,0 +1,101 @@
+"""The C ABI library loads and exports every symbol include/attn_varlen.h
+declares; argument checks that return before any CUDA call; the binding's
+symbol table matches the header.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import variable_length_prefill_gb300 as vlp
+from variable_length_prefill_gb300 import _binding as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "attn_varlen.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"\b(attn_varlen_\w+)\s*\(", src))
+
+
+def _codes():
+    src = open(HEADER).read()
+    return {m.group(1): int(m.group(2))
+            for m in re.finditer(r"#define\s+ATTN_VARLEN_(\w+)\s+(-?\d+)", src)}
+
+
+def test_library_exports_every_declared_symbol():
+    lib = vlp.load()
+    declared = _declared()
+    assert declared == set(B.SYMBOLS), (declared, set(B.SYMBOLS))
+    for name in declared:
+        assert hasattr(lib, name)
+
+
+def test_return_codes_match_header():
+    codes = _codes()
+    assert codes["OK"] == B.OK
+    for name in ("INVALID_ARG", "UNSUPPORTED_DIM", "MISALIGNED", "UNSUPPORTED_DEVICE",
+                 "CUDA", "OOM", "DEVICE_TIMEOUT", "WORKSPACE_SMALL", "DRIVER"):
+        assert codes["ERR_" + name] == getattr(B, "ERR_" + name)
+    for c in codes.values():
+        assert vlp.strerror(c) != "unknown error code"
+    assert vlp.strerror(12345) == "unknown error code"
+
+
+def test_version_and_workspace_size():
+    lib = vlp.load()
+    assert lib.attn_varlen_version() >= 100
+    assert vlp.workspace_size(-1) == 0
+    sizes = [vlp.workspace_size(n) for n in (0, 1, 9, 1000, 100000)]
+    assert sizes == sorted(sizes) and all(s % 256 == 0 for s in sizes)
+    # 3 tensor maps of 128 B per sequence plus order/prefix arrays
+    assert vlp.workspace_size(1000) >= 1000 * 3 * 128 + 2 * 1000 * 4
+
+
+P = 0x100000  # a fake, 16-byte aligned address; never dereferenced
+
+
+@pytest.mark.parametrize("args,code", [
+    # num_seqs < 0
+    ((P, P, P, P, P, -1, 4, 72, P, None), B.ERR_INVALID_ARG),
+    # num_heads < 1
+    ((P, P, P, P, P, 1, 0, 72, P, None), B.ERR_INVALID_ARG),
+    # head_dim not 72/128
+    ((P, P, P, P, P, 1, 4, 64, P, None), B.ERR_UNSUPPORTED_DIM),
+    ((P, P, P, P, P, 1, 4, 80, P, None), B.ERR_UNSUPPORTED_DIM),
+    # null pointers
+    ((None, P, P, P, P, 1, 4, 72, P, None), B.ERR_INVALID_ARG),
+    ((P, P, P, P, None, 1, 4, 128, P, None), B.ERR_INVALID_ARG),
+    ((P, P, P, P, P, 1, 4, 128, None, None), B.ERR_INVALID_ARG),
+    # misaligned bf16 buffers / cu_seqlens
+    ((P + 8, P, P, P, P, 1, 4, 72, P, None), B.ERR_MISALIGNED),
+    ((P, P, P, P, P, 1, 4, 72, P + 2, None), B.ERR_MISALIGNED),
+    ((P, P, P, P + 2, P, 1, 4, 72, P, None), B.ERR_MISALIGNED),
+    # num_seqs == 0 is a no-op, even with null pointers
+    ((None, None, None, None, None, 0, 4, 72, None, None), B.OK),
+])
+def test_argument_checks_need_no_gpu(args, code):
+    assert vlp.load().attn_varlen_fwd(*args) == code
+
+
+def test_workspace_variant_checks():
+    lib = vlp.load()
+    need = vlp.workspace_size(2)
+    assert lib.attn_varlen_fwd_ws(P, P, P, P, P, 2, 4, 72, P, None, need, None) == B.ERR_INVALID_ARG
+    assert lib.attn_varlen_fwd_ws(P, P, P, P, P, 2, 4, 72, P, P + 16, need, None) == B.ERR_MISALIGNED
+    assert lib.attn_varlen_fwd_ws(P, P, P, P, P, 2, 4, 72, P, P, need - 1, None) == B.ERR_WORKSPACE_SMALL
+    assert lib.attn_varlen_check_ws(None, None) == B.ERR_INVALID_ARG
+
+
+def test_product_path_has_no_oracle_dependency():
+    """The package never imports the CPU oracle."""
+    pkg = os.path.dirname(vlp.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "attn_oracle" not in text, f

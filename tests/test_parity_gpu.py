@@ -1,0 +1,141 @@
+"""CUDA path (through the C ABI) against the CPU oracle, element by element on
+seeded inputs: the five workloads, ragged tiles, varlen edge cases, and
+properties that hold at any size."""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_helpers import (assert_close, check_full, check_sampled, device_inputs, run_cuda,
+                         to_bits)
+from workloads import C1, C2, C3, C4, C5, Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    # (lens_q, lens_k or None, heads, head_dim)
+    ((1,), None, 1, 72), ((1,), None, 1, 128),
+    ((127,), None, 2, 72), ((128,), None, 2, 128), ((129,), None, 2, 72),
+    ((255,), None, 2, 128), ((256,), None, 2, 72), ((257,), None, 2, 128),
+    ((300,), None, 2, 72), ((513,), None, 2, 128), ((700,), None, 3, 72),
+    ((5, 130, 0, 257, 1, 64), None, 3, 72), ((5, 130, 0, 257, 1, 64), None, 3, 128),
+    ((100, 300, 7), (257, 64, 1000), 2, 72), ((100, 300, 7), (257, 64, 1000), 2, 128),
+    ((10, 5, 3), (0, 7, 0), 2, 72),
+]
+
+
+@pytest.mark.parametrize("lens_q,lens_k,H,D", SMALL)
+def test_small_ragged_shapes(cuda_lib, lens_q, lens_k, H, D):
+    w = Workload(f"small_{lens_q}_{lens_k}_{H}_{D}", lens_q, H, D, seed=100 + sum(lens_q) + D,
+                 seq_lens_k=lens_k)
+    check_full(cuda_lib, w)
+
+
+def test_c1_all_rows(cuda_lib):
+    check_full(cuda_lib, C1)
+
+
+def test_c5_all_rows(cuda_lib):
+    check_full(cuda_lib, C5)
+
+
+@pytest.mark.parametrize("w,rows", [(C2, 512), (C3, 512), (C4, 512)], ids=lambda x: getattr(x, "name", str(x)))
+def test_full_size_sampled_rows(cuda_lib, w, rows):
+    check_sampled(cuda_lib, w, rows)
+
+
+def test_lk_zero_gives_zero_rows(cuda_lib):
+    w = Workload("lk0", (10, 5, 3), 2, 72, seed=41, seq_lens_k=(0, 7, 0))
+    x = make_inputs(w)
+    got = run_cuda(cuda_lib, x)
+    assert (got[0:10] == 0).all() and (got[15:18] == 0).all()
+    assert (got[10:15] != 0).any()
+
+
+def test_rows_outside_sequences_untouched(cuda_lib):
+    """cu_seqlens starting past row 0, an empty sequence, and rows after the
+    last sequence: a sentinel pattern there must survive bit for bit."""
+    w = Workload("offsets", (40, 0, 200, 3), 2, 128, seed=42, cu_offset=7)
+    x = make_inputs(w)
+    # two extra trailing rows beyond cu_q[-1]
+    for n in ("q", "k", "v"):
+        x[n] = np.concatenate([x[n], np.ones((2,) + x[n].shape[1:], np.uint16)])
+    sentinel = 0x7FC1  # a NaN payload the kernel never produces
+    got = run_cuda(cuda_lib, x, out_fill=sentinel)
+    cu = x["cu_q"]
+    assert (got[:cu[0]] == sentinel).all()
+    assert (got[cu[-1]:] == sentinel).all()
+    ref = oracle.attn_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"])
+    assert_close(got[cu[0]:cu[-1]], ref[cu[0]:cu[-1]], "offsets")
+
+
+def test_num_seqs_zero_is_a_noop(cuda_lib):
+    import torch
+    q = torch.zeros(4, 2, 72, dtype=torch.bfloat16, device="cuda")
+    cu = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full_like(q, 3.0)
+    cuda_lib.attn_varlen_fwd(q, q, q, cu, cu, out=out)
+    cuda_lib.check()
+    assert (out == 3.0).all()
+
+
+def test_packing_invariance_bitwise(cuda_lib):
+    """The packed batch equals each member run alone, bit for bit (tiles
+    start at sequence starts, so every row sees the same arithmetic)."""
+    x = make_inputs(C5)
+    packed = run_cuda(cuda_lib, x)
+    cu = x["cu_q"]
+    for i in range(len(cu) - 1):
+        if cu[i + 1] <= cu[i]:
+            continue
+        sl = slice(cu[i], cu[i + 1])
+        alone = {"q": x["q"][sl], "k": x["k"][sl], "v": x["v"][sl],
+                 "cu_q": np.array([0, cu[i + 1] - cu[i]], np.int32),
+                 "cu_k": np.array([0, cu[i + 1] - cu[i]], np.int32)}
+        np.testing.assert_array_equal(run_cuda(cuda_lib, alone), packed[sl])
+
+
+def test_deterministic(cuda_lib):
+    x = make_inputs(C5)
+    np.testing.assert_array_equal(run_cuda(cuda_lib, x), run_cuda(cuda_lib, x))
+
+
+def test_many_short_sequences(cuda_lib):
+    """300 sequences (some empty) plus one long one: longest-first order and
+    the unit search over many sequences."""
+    rng = np.random.default_rng(43)
+    lens = tuple(int(v) for v in rng.integers(0, 5, 300)) + (1500,)
+    check_full(cuda_lib, Workload("many_short", lens, 2, 72, seed=44))
+
+
+def test_more_sequences_than_sorted_limit(cuda_lib):
+    """Beyond the longest-first limit the natural order is used."""
+    rng = np.random.default_rng(45)
+    lens = tuple(int(v) for v in rng.integers(0, 4, 2500))
+    check_full(cuda_lib, Workload("very_many", lens, 1, 128, seed=46))
+
+
+def test_caller_workspace_on_two_streams(cuda_lib):
+    import torch
+    x = make_inputs(C1)
+    want = run_cuda(cuda_lib, x)
+    t, cu_q, cu_k = device_inputs(x, "cuda")
+    outs = []
+    for _ in range(2):
+        s = torch.cuda.Stream()
+        ws = torch.zeros(cuda_lib.workspace_size(1), dtype=torch.uint8, device="cuda")
+        with torch.cuda.stream(s):
+            out = cuda_lib.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, workspace=ws)
+        outs.append((s, ws, out))
+    for s, ws, out in outs:
+        cuda_lib.check(stream=s, workspace=ws)
+        np.testing.assert_array_equal(to_bits(out), want)
+
+
+def test_errors_raise(cuda_lib):
+    import torch
+    from variable_length_prefill_gb300 import AttnVarlenError
+    q = torch.zeros(8, 2, 64, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 8], dtype=torch.int32, device="cuda")
+    with pytest.raises(AttnVarlenError) as e:
+        cuda_lib.attn_varlen_fwd(q, q, q, cu, cu)
+    assert e.value.code == -2

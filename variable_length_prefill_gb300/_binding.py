@@ -1,0 +1,146 @@
+"""ctypes binding of the C ABI in include/attn_varlen.h.
+
+Argument marshalling only: every step of the attention runs in the CUDA
+library.  There is no fallback -- if the in-tree library cannot be built or
+loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import build as _build
+
+# Return codes (include/attn_varlen.h)
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED_DIM = -2
+ERR_MISALIGNED = -3
+ERR_UNSUPPORTED_DEVICE = -4
+ERR_CUDA = -5
+ERR_OOM = -6
+ERR_DEVICE_TIMEOUT = -7
+ERR_WORKSPACE_SMALL = -8
+ERR_DRIVER = -9
+
+# Every symbol the header declares, with (restype, argtypes).
+_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SYMBOLS = {
+    "attn_varlen_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "attn_varlen_workspace_size": (_SZ, [_I]),
+    "attn_varlen_fwd_ws": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _SZ, _P]),
+    "attn_varlen_check": (_I, [_P]),
+    "attn_varlen_check_ws": (_I, [_P, _P]),
+    "attn_varlen_strerror": (ctypes.c_char_p, [_I]),
+    "attn_varlen_version": (_I, []),
+}
+
+_LOCK = threading.Lock()
+_LIB = None
+
+
+class AttnVarlenError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (code {code})")
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load the in-tree CUDA library (building it first when absent)."""
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            path = _build.lib_path()
+            if build_if_missing:
+                path = _build.build()
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SYMBOLS.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _LIB = lib
+        return _LIB
+
+
+def strerror(code: int) -> str:
+    return load().attn_varlen_strerror(int(code)).decode()
+
+
+def workspace_size(num_seqs: int) -> int:
+    return int(load().attn_varlen_workspace_size(int(num_seqs)))
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def _check_inputs(q, k, v, cu_q, cu_k, out):
+    import torch
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("q, k, v must be bfloat16")
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape:
+        raise ValueError("q, k, v must be [total_tokens, num_heads, head_dim]; k and v alike")
+    if q.shape[1:] != k.shape[1:]:
+        raise ValueError("q and k must share num_heads and head_dim")
+    for t in (q, k, v, out):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v and out must be contiguous CUDA tensors")
+    if cu_q.dtype != torch.int32 or cu_k.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if cu_q.dim() != 1 or cu_q.shape != cu_k.shape or cu_q.numel() < 1:
+        raise ValueError("cu_seqlens_q/k must be 1-D, equal length, >= 1 entry")
+    if not cu_q.is_cuda or not cu_k.is_cuda or not cu_q.is_contiguous() or not cu_k.is_contiguous():
+        raise ValueError("cu_seqlens must be contiguous CUDA tensors")
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must have q's shape and dtype")
+
+
+def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, out=None, stream=None,
+                    workspace=None):
+    """softmax(q k^T / sqrt(head_dim)) v per packed sequence and head.
+
+    q: bf16 [total_q, H, D]; k, v: bf16 [total_k, H, D]; cu_seqlens_q/k:
+    int32 [num_seqs + 1] on the same device.  Returns ``out`` (allocated with
+    ``torch.empty_like(q)`` when not given; rows outside every query slice are
+    left untouched).  ``workspace``: optional uint8 CUDA tensor of at least
+    ``workspace_size(num_seqs)`` bytes, zero-filled before first use.
+    """
+    import torch
+    if out is None:
+        out = torch.empty_like(q)
+    _check_inputs(q, k, v, cu_seqlens_q, cu_seqlens_k, out)
+    lib = load()
+    num_seqs = cu_seqlens_q.numel() - 1
+    H, D = q.shape[1], q.shape[2]
+    s = _stream_handle(stream, q.device)
+    with torch.cuda.device(q.device):
+        if workspace is None:
+            rc = lib.attn_varlen_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                     cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+                                     num_seqs, H, D, out.data_ptr(), s)
+        else:
+            rc = lib.attn_varlen_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                        cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+                                        num_seqs, H, D, out.data_ptr(), workspace.data_ptr(),
+                                        workspace.numel() * workspace.element_size(), s)
+    if rc != OK:
+        raise AttnVarlenError(rc, "attn_varlen_fwd")
+    return out
+
+
+def check(stream=None, device=None, workspace=None) -> int:
+    """Synchronise and return (and clear) the device status; raises on error."""
+    import torch
+    dev = device if device is not None else torch.cuda.current_device()
+    s = _stream_handle(stream, dev)
+    with torch.cuda.device(dev):
+        if workspace is None:
+            rc = load().attn_varlen_check(s)
+        else:
+            rc = load().attn_varlen_check_ws(workspace.data_ptr(), s)
+    if rc != OK:
+        raise AttnVarlenError(rc, "attn_varlen_check")
+    return rc

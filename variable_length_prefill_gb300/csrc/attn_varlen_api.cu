@@ -1,0 +1,268 @@
+// C ABI of the packed variable-length attention forward (declared in
+// include/attn_varlen.h): argument checks, the per-device workspace, the
+// tensor-map templates and the two launches.  No step of the computation runs
+// on the host; cu_seqlens stay on the device.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn_varlen.h"
+#include "attn_varlen_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool probed = false;
+  bool supported = false;
+  bool prepared[2] = {false, false};  // kernel attributes for head_dim 72, 128
+  int sm_count = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_probed = false;
+
+int map_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_VARLEN_OK : ATTN_VARLEN_ERR_CUDA; }
+
+// Called with g_mu held.
+int probe_device(int dev, DeviceState& st) {
+  if (st.probed) return st.supported ? ATTN_VARLEN_OK : ATTN_VARLEN_ERR_UNSUPPORTED_DEVICE;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return ATTN_VARLEN_ERR_CUDA;
+  st.probed = true;
+  st.supported = (major == 10 && minor == 3);
+  st.sm_count = sms;
+  return st.supported ? ATTN_VARLEN_OK : ATTN_VARLEN_ERR_UNSUPPORTED_DEVICE;
+}
+
+// Called with g_mu held.
+int get_encoder() {
+  if (!g_encode_probed) {
+    g_encode_probed = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode ? ATTN_VARLEN_OK : ATTN_VARLEN_ERR_DRIVER;
+}
+
+int check_args(const void* q, const void* k, const void* v, const int32_t* cu_q,
+               const int32_t* cu_k, int num_seqs, int num_heads, int head_dim, const void* out) {
+  if (num_seqs < 0 || num_heads < 1) return ATTN_VARLEN_ERR_INVALID_ARG;
+  if (head_dim != 72 && head_dim != 128) return ATTN_VARLEN_ERR_UNSUPPORTED_DIM;
+  if (num_seqs == 0) return ATTN_VARLEN_OK;
+  if (!q || !k || !v || !cu_q || !cu_k || !out) return ATTN_VARLEN_ERR_INVALID_ARG;
+  const uintptr_t mis = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) &
+                        15u;
+  if (mis) return ATTN_VARLEN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(cu_q) | reinterpret_cast<uintptr_t>(cu_k)) & 3u)
+    return ATTN_VARLEN_ERR_MISALIGNED;
+  // token stride must fit the tensor-map stride field (< 2^40 bytes)
+  if ((uint64_t)num_heads * (uint64_t)head_dim * 2u >= (1ull << 40)) return ATTN_VARLEN_ERR_INVALID_ARG;
+  return ATTN_VARLEN_OK;
+}
+
+// Host-encoded template: a 3-D bf16 map {head_dim, num_heads, rows} with box
+// {box, 1, 128}; the plan kernel patches the address and the row extent per
+// sequence.
+int encode_template(CUtensorMap* m, const void* base, int num_heads, int head_dim) {
+  const int box = avp::box_cols(head_dim);
+  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads, (cuuint64_t)avp::kBlockM};
+  cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_heads * head_dim * 2};
+  cuuint32_t boxdim[3] = {(cuuint32_t)box, 1, (cuuint32_t)avp::kBlockM};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle swz =
+      avp::box_swizzle_128(head_dim) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B;
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, boxdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_VARLEN_OK : ATTN_VARLEN_ERR_DRIVER;
+}
+
+int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const int32_t* cu_k,
+        int num_seqs, int num_heads, int head_dim, void* out, void* ws, int dev,
+        DeviceState& st, cudaStream_t stream) {
+  avp::PlanParams pp;
+  std::memset(&pp, 0, sizeof(pp));
+  const void* bases[3] = {q, k, v};
+  for (int m = 0; m < avp::kMapsPerSeq; ++m) {
+    int rc = encode_template(&pp.tmpl[m], bases[m], num_heads, head_dim);
+    if (rc) return rc;
+    pp.base[m] = static_cast<const uint8_t*>(bases[m]);
+  }
+  pp.cu_q = cu_q;
+  pp.cu_k = cu_k;
+  pp.ws = static_cast<uint8_t*>(ws);
+  pp.num_seqs = num_seqs;
+  pp.num_heads = num_heads;
+  pp.row_bytes = num_heads * head_dim * 2;
+
+  avp::FwdParams fp;
+  fp.ws = static_cast<const uint8_t*>(ws);
+  fp.status = static_cast<int*>(ws);
+  fp.cu_q = cu_q;
+  fp.cu_k = cu_k;
+  fp.out = static_cast<uint16_t*>(out);
+  fp.num_seqs = num_seqs;
+  fp.num_heads = num_heads;
+  fp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
+
+  const int slot = head_dim == 72 ? 0 : 1;
+  if (!st.prepared[slot]) {
+    if (avp::prepare_fwd(head_dim) != cudaSuccess) return ATTN_VARLEN_ERR_CUDA;
+    st.prepared[slot] = true;
+  }
+  (void)dev;
+  cudaError_t e = avp::launch_plan(pp, stream);
+  if (e != cudaSuccess) return ATTN_VARLEN_ERR_CUDA;
+  e = avp::launch_fwd(head_dim, fp, st.sm_count, stream);
+  return map_cuda(e);
+}
+
+// Grow the library-owned workspace of `dev` (g_mu held).  Keeps the status
+// word across the reallocation.
+int ensure_workspace(DeviceState& st, size_t need) {
+  if (st.ws && st.ws_bytes >= need) return ATTN_VARLEN_OK;
+  size_t bytes = need < (1u << 16) ? (1u << 16) : need + need / 2;
+  bytes = (bytes + 255) & ~(size_t)255;
+  int status = 0;
+  if (st.ws) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_VARLEN_ERR_CUDA;
+    if (cudaMemcpy(&status, st.ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return ATTN_VARLEN_ERR_CUDA;
+    cudaFree(st.ws);
+    st.ws = nullptr;
+    st.ws_bytes = 0;
+  }
+  void* p = nullptr;
+  if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_VARLEN_ERR_OOM;
+  }
+  if (cudaMemset(p, 0, 256) != cudaSuccess ||
+      cudaMemcpy(p, &status, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(p);
+    return ATTN_VARLEN_ERR_CUDA;
+  }
+  st.ws = p;
+  st.ws_bytes = bytes;
+  return ATTN_VARLEN_OK;
+}
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return ATTN_VARLEN_ERR_CUDA;
+  if (*dev < 0 || *dev >= kMaxDevices) return ATTN_VARLEN_ERR_UNSUPPORTED_DEVICE;
+  return ATTN_VARLEN_OK;
+}
+
+int read_and_clear_status(void* ws, cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_VARLEN_ERR_CUDA;
+  int status = 0;
+  if (cudaMemcpy(&status, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_VARLEN_ERR_CUDA;
+  if (status != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return ATTN_VARLEN_ERR_CUDA;
+    return ATTN_VARLEN_ERR_DEVICE_TIMEOUT;
+  }
+  return ATTN_VARLEN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_varlen_workspace_size(int num_seqs) {
+  if (num_seqs < 0) return 0;
+  return avp::ws_layout(num_seqs).total;
+}
+
+int attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                    const int32_t* cu_seqlens_k, int num_seqs, int num_heads, int head_dim,
+                    void* out, cudaStream_t stream) {
+  int rc = check_args(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out);
+  if (rc || num_seqs == 0) return rc;
+  int dev = 0;
+  if ((rc = current_device(&dev))) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if ((rc = probe_device(dev, st))) return rc;
+  if ((rc = get_encoder())) return rc;
+  if ((rc = ensure_workspace(st, avp::ws_layout(num_seqs).total))) return rc;
+  return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, st.ws, dev,
+             st, stream);
+}
+
+int attn_varlen_fwd_ws(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                       const int32_t* cu_seqlens_k, int num_seqs, int num_heads, int head_dim,
+                       void* out, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_args(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out);
+  if (rc || num_seqs == 0) return rc;
+  if (!workspace) return ATTN_VARLEN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_VARLEN_ERR_MISALIGNED;
+  if (workspace_bytes < avp::ws_layout(num_seqs).total) return ATTN_VARLEN_ERR_WORKSPACE_SMALL;
+  int dev = 0;
+  if ((rc = current_device(&dev))) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if ((rc = probe_device(dev, st))) return rc;
+  if ((rc = get_encoder())) return rc;
+  return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, workspace,
+             dev, st, stream);
+}
+
+int attn_varlen_check(cudaStream_t stream) {
+  int dev = 0;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    ws = g_dev[dev].ws;
+  }
+  if (!ws) return cudaStreamSynchronize(stream) == cudaSuccess ? ATTN_VARLEN_OK : ATTN_VARLEN_ERR_CUDA;
+  return read_and_clear_status(ws, stream);
+}
+
+int attn_varlen_check_ws(void* workspace, cudaStream_t stream) {
+  if (!workspace) return ATTN_VARLEN_ERR_INVALID_ARG;
+  return read_and_clear_status(workspace, stream);
+}
+
+const char* attn_varlen_strerror(int code) {
+  switch (code) {
+    case ATTN_VARLEN_OK: return "ok";
+    case ATTN_VARLEN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_VARLEN_ERR_UNSUPPORTED_DIM: return "head_dim must be 72 or 128";
+    case ATTN_VARLEN_ERR_MISALIGNED: return "q, k, v and out must be 16-byte aligned (cu_seqlens 4-byte)";
+    case ATTN_VARLEN_ERR_UNSUPPORTED_DEVICE: return "current device is not sm_103 (GB300)";
+    case ATTN_VARLEN_ERR_CUDA: return "CUDA runtime error";
+    case ATTN_VARLEN_ERR_OOM: return "workspace allocation failed";
+    case ATTN_VARLEN_ERR_DEVICE_TIMEOUT: return "a kernel wait ran out of time";
+    case ATTN_VARLEN_ERR_WORKSPACE_SMALL: return "workspace smaller than attn_varlen_workspace_size()";
+    case ATTN_VARLEN_ERR_DRIVER: return "cuTensorMapEncodeTiled unavailable or failed";
+    default: return "unknown error code";
+  }
+}
+
+int attn_varlen_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// Internal layout shared by the host library and the kernels: the workspace,
+// the launch parameters and the fixed tiling.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace avp {
+
+// Tiling: a work unit is (sequence, head, 256 query rows) = two 128-row Q
+// tiles that share every K/V tile; keys stream in tiles of 128.
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+constexpr int kUnitRows = 2 * kBlockM;
+constexpr int kMapsPerSeq = 3;       // q, k, v tensor maps per sequence
+constexpr int kMapBytes = 128;       // sizeof(CUtensorMap)
+constexpr int kLptMaxSeqs = 2048;    // longest-first ordering up to this many sequences
+
+// Device status word bits (sticky until read by the check call).
+constexpr int kStatusTimeoutLoad = 1;
+constexpr int kStatusTimeoutMma = 2;
+constexpr int kStatusTimeoutSoftmax = 4;
+
+// Workspace: [header 256 B][tensor maps][order int32 N][prefix int32 N+1]
+//   header: int32 status, int32 num_units
+struct WsLayout {
+  size_t maps;
+  size_t order;
+  size_t prefix;
+  size_t total;
+};
+
+__host__ __device__ inline WsLayout ws_layout(int num_seqs) {
+  const size_t n = num_seqs > 0 ? (size_t)num_seqs : 0;
+  WsLayout w;
+  w.maps = 256;
+  w.order = ((w.maps + n * kMapsPerSeq * kMapBytes + 255) / 256) * 256;
+  w.prefix = w.order + ((n * 4 + 255) / 256) * 256;
+  w.total = w.prefix + (((n + 1) * 4 + 255) / 256) * 256;
+  return w;
+}
+
+struct PlanParams {
+  CUtensorMap tmpl[kMapsPerSeq];  // host-encoded q/k/v templates (address, extent patched)
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const uint8_t* base[kMapsPerSeq];  // q, k, v
+  uint8_t* ws;
+  int num_seqs;
+  int num_heads;
+  int row_bytes;  // num_heads * head_dim * 2
+};
+
+struct FwdParams {
+  const uint8_t* ws;
+  int* status;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  uint16_t* out;
+  int num_seqs;
+  int num_heads;
+  float scale_log2;  // head_dim^-1/2 * log2(e)
+};
+
+// Kernel launchers (attn_varlen_kernels.cu).
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
+cudaError_t prepare_fwd(int head_dim);  // per device, before the first launch
+cudaError_t launch_fwd(int head_dim, const FwdParams& p, int grid, cudaStream_t stream);
+int fwd_threads();
+size_t fwd_smem_bytes(int head_dim);
+int box_cols(int head_dim);  // TMA box width in columns for this head_dim
+bool box_swizzle_128(int head_dim);
+
+}  // namespace avp

@@ -1,0 +1,661 @@
+// Packed variable-length, non-causal attention forward for sm_103a.
+//
+// What is computed: atrex-bench "attention_forward" (page #001, reference.py,
+// Model.forward) -- per non-empty query sequence and head,
+// softmax(Q K^T * head_dim^-1/2) V over that sequence's keys, bf16 in, bf16
+// out, fp32 accumulation.
+//
+// Two kernels run back to back on the caller's stream:
+//
+//  1. plan (one CTA): reads cu_seqlens on the device, counts the work units
+//     of every sequence (a unit is one head x 256 query rows), orders the
+//     sequences longest-key-range first, writes the prefix sums of the units
+//     in that order, and writes one q, one k and one v tensor map per
+//     sequence by patching host-encoded templates (global address = the
+//     sequence's first row, row extent = the sequence length) so that TMA
+//     zero-fills every row past the end of a sequence.
+//
+//  2. fwd (persistent, one CTA per SM, 10 warps): each CTA walks the unit
+//     list with a stride of gridDim.x.  Warp roles:
+//       warps 0-3  softmax for Q tile 0 (TMEM lanes 0-127 = its 128 rows)
+//       warps 4-7  softmax for Q tile 1
+//       warp  8    TMA producer: Q tiles, then a ring of K and V tiles
+//       warp  9    TMEM owner and tcgen05.mma issuer
+//     TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+DP),
+//     O1 [384,384+DP); P (bf16, packed in pairs) overwrites the first 64
+//     columns of its S and is the A operand of the P.V MMA straight from TMEM.
+//     The MMA issue order alternates the two Q tiles,
+//       S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
+//     so each softmax warpgroup has the other tile's two MMAs to hide behind.
+//     Softmax is an online exp2 softmax, one row per thread, with a lazy
+//     rescale: the running max is only raised (and O rescaled in TMEM) when a
+//     row's new max exceeds it by more than kRescaleThreshold (log2 units).
+//
+// Head dims: 128 runs natively (two 64-column TMA boxes, 128-byte swizzle);
+// 72 is padded to 80 (five 16-column boxes, 32-byte swizzle; TMA zero-fills
+// columns 72-79 of Q and K, so they add nothing to Q.K^T, and the padded
+// output columns are never stored).  The scale always uses the true head_dim.
+//
+// Every mbarrier wait is bounded in time; a wait that runs out records a bit
+// in the workspace status word, raises a CTA-wide abort flag, and the CTA
+// drains its outstanding copies and MMAs (again with a bound), frees TMEM
+// and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "attn_varlen_internal.h"
+#include "ptx.cuh"
+
+namespace avp {
+
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
+
+template <int D>
+struct Cfg;
+template <>
+struct Cfg<72> {
+  static constexpr int DP = 80;   // padded head_dim (MMA K and N multiple of 16)
+  static constexpr int BW = 16;   // columns per TMA box
+  static constexpr int STAGES = 6;
+  static constexpr uint32_t SWZ = kSwizzle32B;
+};
+template <>
+struct Cfg<128> {
+  static constexpr int DP = 128;
+  static constexpr int BW = 64;
+  static constexpr int STAGES = 4;
+  static constexpr uint32_t SWZ = kSwizzle128B;
+};
+
+template <int D>
+struct Geometry {
+  static constexpr int DP = Cfg<D>::DP;
+  static constexpr int BW = Cfg<D>::BW;
+  static constexpr int NB = DP / BW;                        // boxes per tile
+  static constexpr int STAGES = Cfg<D>::STAGES;
+  static constexpr uint32_t SWZ = Cfg<D>::SWZ;
+  static constexpr uint32_t BOX_BYTES = kBlockM * BW * 2;   // one box: 128 rows x BW
+  static constexpr uint32_t TILE_BYTES = kBlockM * DP * 2;  // one Q/K/V tile
+  static constexpr uint32_t SBO = 8 * BW * 2;               // 8-row group stride
+  static constexpr uint32_t Q_OFF = 0;
+  static constexpr uint32_t KV_OFF = 2 * TILE_BYTES;
+  static constexpr uint32_t BAR_OFF = KV_OFF + STAGES * TILE_BYTES;
+  // barrier slots (8 bytes each)
+  static constexpr int B_Q_FULL = 0, B_Q_EMPTY = 1, B_KV_FULL = 2, B_KV_EMPTY = 2 + STAGES,
+                       B_S_FULL = 2 + 2 * STAGES, B_P_FULL = B_S_FULL + 2,
+                       B_PV_DONE = B_P_FULL + 2, B_DRAIN = B_PV_DONE + 2, NUM_BARS = B_DRAIN + 1;
+  static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // tmem slot, abort flag
+  static constexpr uint32_t SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
+  static constexpr int NK_S = DP / 16;        // K-steps of S = Q K^T
+  static constexpr int NK_PV = kBlockN / 16;  // K-steps of O += P V
+  static constexpr uint32_t S_COL0 = 0, O_COL0 = 256;
+};
+
+struct UnitInfo {
+  int seq, head, q0, lq, lk, qbase, nkv;
+  bool t1;  // second Q tile holds at least one row
+};
+
+__device__ __forceinline__ UnitInfo decode_unit(int u, const int32_t* __restrict__ order,
+                                                const int32_t* __restrict__ prefix, int num_seqs,
+                                                const int32_t* __restrict__ cu_q,
+                                                const int32_t* __restrict__ cu_k) {
+  // largest rank r in [0, num_seqs) with prefix[r] <= u
+  int lo = 0, hi = num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(prefix + mid) <= u) lo = mid; else hi = mid - 1;
+  }
+  UnitInfo ui;
+  ui.seq = __ldg(order + lo);
+  const int local = u - __ldg(prefix + lo);
+  ui.qbase = __ldg(cu_q + ui.seq);
+  ui.lq = __ldg(cu_q + ui.seq + 1) - ui.qbase;
+  const int kb = __ldg(cu_k + ui.seq);
+  ui.lk = __ldg(cu_k + ui.seq + 1) - kb;
+  if (ui.lk < 0) ui.lk = 0;
+  const int pairs = (ui.lq + kUnitRows - 1) / kUnitRows;
+  ui.head = local / pairs;
+  ui.q0 = (local - ui.head * pairs) * kUnitRows;
+  ui.t1 = ui.q0 + kBlockM < ui.lq;
+  ui.nkv = (ui.lk + kBlockN - 1) / kBlockN;
+  return ui;
+}
+
+// Bounded wait: spins on the barrier, gives up after kWaitLimitNs or as soon
+// as another role of the CTA has given up.  Returns false on give-up.
+__device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, int* status, int code) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(status, code);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             int* status, int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bounded_slow(bar, parity, abort_flag, status, code);
+}
+
+// Wait with a fixed bound and no abort check (used only while draining).
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------- plan
+__global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_constant__ PlanParams p) {
+  __shared__ int s_key[kLptMaxSeqs];
+  __shared__ int s_warp[32];
+  __shared__ int s_carry;
+  const int N = p.num_seqs;
+  const WsLayout L = ws_layout(N);
+  int* hdr = reinterpret_cast<int*>(p.ws);
+  int* order = reinterpret_cast<int*>(p.ws + L.order);
+  int* prefix = reinterpret_cast<int*>(p.ws + L.prefix);
+  const bool lpt = N <= kLptMaxSeqs;
+  const int tid = threadIdx.x, nt = blockDim.x;
+
+  // 1. per sequence: sort key, tensor maps
+  bool wrote_map = false;
+  for (int i = tid; i < N; i += nt) {
+    const int q0 = p.cu_q[i], lq = p.cu_q[i + 1] - q0;
+    const int k0 = p.cu_k[i], lk = p.cu_k[i + 1] - k0;
+    const bool live = lq > 0;
+    if (lpt) s_key[i] = live ? (lk > 0 ? lk : 0) : -1;
+    if (live && lk > 0) {
+      for (int m = 0; m < kMapsPerSeq; ++m) {
+        uint8_t* dst = p.ws + L.maps + ((size_t)i * kMapsPerSeq + m) * kMapBytes;
+        const uint4* src = reinterpret_cast<const uint4*>(&p.tmpl[m]);
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int w = 0; w < kMapBytes / 16; ++w) d4[w] = src[w];
+        const int row0 = (m == 0) ? q0 : k0;
+        const int len = (m == 0) ? lq : lk;
+        tmap_set_address(dst, p.base[m] + (size_t)row0 * p.row_bytes);
+        tmap_set_dim2(dst, (uint32_t)len);
+      }
+      wrote_map = true;
+    }
+  }
+  if (wrote_map) tmap_release();
+  __syncthreads();
+
+  // 2. rank = position in longest-key-range-first order (stable)
+  for (int i = tid; i < N; i += nt) {
+    int rank = i;
+    if (lpt) {
+      const int ki = s_key[i];
+      rank = 0;
+      for (int j = 0; j < N; ++j) {
+        const int kj = s_key[j];
+        rank += (kj > ki) || (kj == ki && j < i);
+      }
+    }
+    order[rank] = i;
+  }
+  __syncthreads();
+
+  // 3. exclusive prefix sums of the unit counts in rank order
+  const int chunk = (N + nt - 1) / nt;
+  const int r0 = tid * chunk, r1 = min(N, r0 + chunk);
+  int local = 0;
+  for (int r = r0; r < r1; ++r) {
+    const int i = order[r];
+    const int lq = p.cu_q[i + 1] - p.cu_q[i];
+    local += lq > 0 ? p.num_heads * ((lq + kUnitRows - 1) / kUnitRows) : 0;
+  }
+  // block-wide exclusive scan of `local`
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = nt >> 5;
+    int w = lane < nw ? s_warp[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < nw) s_warp[lane] = wi - w;  // exclusive warp offsets
+    if (lane == nw - 1) s_carry = wi;      // total
+  }
+  __syncthreads();
+  int run = s_warp[warp] + incl - local;
+  for (int r = r0; r < r1; ++r) {
+    prefix[r] = run;
+    const int i = order[r];
+    const int lq = p.cu_q[i + 1] - p.cu_q[i];
+    run += lq > 0 ? p.num_heads * ((lq + kUnitRows - 1) / kUnitRows) : 0;
+  }
+  if (tid == 0) {
+    prefix[N] = s_carry;
+    hdr[1] = s_carry;
+  }
+}
+
+// -------------------------------------------------------------------- fwd
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using G = Geometry<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_u32);
+  const uint32_t sQ = base + G::Q_OFF;
+  const uint32_t sKV = base + G::KV_OFF;
+  auto bar = [&](int i) -> uint32_t { return base + G::BAR_OFF + 8u * (uint32_t)i; };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base_ptr + G::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + G::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(G::B_Q_FULL), 1);
+    mbar_init(bar(G::B_Q_EMPTY), 1);
+    for (int s = 0; s < G::STAGES; ++s) {
+      mbar_init(bar(G::B_KV_FULL + s), 1);
+      mbar_init(bar(G::B_KV_EMPTY + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(G::B_S_FULL + t), 1);
+      mbar_init(bar(G::B_P_FULL + t), kBlockM);
+      mbar_init(bar(G::B_PV_DONE + t), 1);
+    }
+    mbar_init(bar(G::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(base + G::MISC_OFF, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const WsLayout L = ws_layout(p.num_seqs);
+  const int num_units = reinterpret_cast<const int*>(p.ws)[1];
+  const int32_t* order = reinterpret_cast<const int32_t*>(p.ws + L.order);
+  const int32_t* prefix = reinterpret_cast<const int32_t*>(p.ws + L.prefix);
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t kv_item = 0, q_use = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+        const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k);
+        if (ui.nkv == 0) continue;
+        const uint8_t* mq = p.ws + L.maps + (size_t)ui.seq * kMapsPerSeq * kMapBytes;
+        const uint8_t* mk = mq + kMapBytes;
+        const uint8_t* mv = mq + 2 * kMapBytes;
+        tmap_acquire(mq);
+        tmap_acquire(mk);
+        tmap_acquire(mv);
+        if (!(ok = wait_bounded(bar(G::B_Q_EMPTY), (q_use & 1u) ^ 1u, abort_flag, p.status,
+                                kStatusTimeoutLoad)))
+          break;
+        ++q_use;
+        mbar_arrive_expect_tx(bar(G::B_Q_FULL), (ui.t1 ? 2u : 1u) * G::TILE_BYTES);
+#pragma unroll
+        for (int b = 0; b < G::NB; ++b)
+          tma_load_3d(sQ + b * G::BOX_BYTES, mq, bar(G::B_Q_FULL), b * G::BW, ui.head, ui.q0);
+        if (ui.t1) {
+#pragma unroll
+          for (int b = 0; b < G::NB; ++b)
+            tma_load_3d(sQ + G::TILE_BYTES + b * G::BOX_BYTES, mq, bar(G::B_Q_FULL), b * G::BW,
+                        ui.head, ui.q0 + kBlockM);
+        }
+        for (int j = 0; ok && j < ui.nkv; ++j) {
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t stage = kv_item % G::STAGES;
+            const uint32_t use = kv_item / G::STAGES;
+            if (!(ok = wait_bounded(bar(G::B_KV_EMPTY + stage), (use & 1u) ^ 1u, abort_flag,
+                                    p.status, kStatusTimeoutLoad)))
+              break;
+            mbar_arrive_expect_tx(bar(G::B_KV_FULL + stage), G::TILE_BYTES);
+            const uint8_t* m = which ? mv : mk;
+            const uint32_t dst = sKV + stage * G::TILE_BYTES;
+#pragma unroll
+            for (int b = 0; b < G::NB; ++b)
+              tma_load_3d(dst + b * G::BOX_BYTES, m, bar(G::B_KV_FULL + stage), b * G::BW,
+                          ui.head, j * kBlockN);
+            ++kv_item;
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy already issued land before the CTA can exit
+        if (q_use > 0) wait_drain(bar(G::B_Q_FULL), (q_use - 1) & 1u);
+        const uint32_t first = kv_item > (uint32_t)G::STAGES ? kv_item - G::STAGES : 0;
+        for (uint32_t it = first; it < kv_item; ++it)
+          wait_drain(bar(G::B_KV_FULL + it % G::STAGES), (it / G::STAGES) & 1u);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, G::DP, false, true);
+      uint32_t kv_item = 0, q_use = 0;
+      uint32_t p_wait[2] = {0, 0};  // p_full phases consumed per tile
+      uint32_t pv_cnt[2] = {0, 0};  // P.V groups committed per tile
+      bool ok = true;
+      bool issued = false;
+
+      auto wait_ = [&](uint32_t b, uint32_t parity) -> bool {
+        return wait_bounded(b, parity, abort_flag, p.status, kStatusTimeoutMma);
+      };
+      // S_t = Q_t K^T : K from stage `ks`
+      auto issue_s = [&](int t, uint32_t ks) {
+        const uint32_t qa = sQ + t * G::TILE_BYTES;
+        const uint32_t kb = sKV + ks * G::TILE_BYTES;
+        const uint32_t d = tmem + G::S_COL0 + 128u * t;
+#pragma unroll
+        for (int k = 0; k < G::NK_S; ++k) {
+          const uint32_t off = (k * 16 / G::BW) * G::BOX_BYTES + ((k * 16) % G::BW) * 2;
+          mma_ss(d, smem_desc(qa + off, 16, G::SBO, G::SWZ), smem_desc(kb + off, 16, G::SBO, G::SWZ),
+                 idesc_s, k > 0 ? 1u : 0u);
+        }
+      };
+      // O_t (+)= P_t V : V from stage `vs`, P from TMEM (aliasing S_t)
+      auto issue_pv = [&](int t, uint32_t vs, bool acc) {
+        const uint32_t vb = sKV + vs * G::TILE_BYTES;
+        const uint32_t d = tmem + G::O_COL0 + 128u * t;
+        const uint32_t a = tmem + G::S_COL0 + 128u * t;
+#pragma unroll
+        for (int k = 0; k < G::NK_PV; ++k) {
+          const uint64_t bdesc = smem_desc(vb + k * 16 * G::BW * 2, G::BOX_BYTES, G::SBO, G::SWZ);
+          mma_ts(d, a + 8u * k, bdesc, idesc_pv, (acc || k > 0) ? 1u : 0u);
+        }
+      };
+      // S_t overwrites P_t: the P.V MMA that reads P_t must be finished
+      auto wait_pv_idle = [&](int t) -> bool {
+        if (pv_cnt[t] == 0) return true;
+        if (!wait_(bar(G::B_PV_DONE + t), (pv_cnt[t] - 1) & 1u)) return false;
+        return true;
+      };
+
+      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+        const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k);
+        if (ui.nkv == 0) continue;
+        if (!(ok = wait_(bar(G::B_Q_FULL), q_use & 1u))) break;
+        ++q_use;
+        // j = 0: S0, S1 from K_0
+        {
+          const uint32_t it = kv_item;
+          if (!(ok = wait_(bar(G::B_KV_FULL + it % G::STAGES), (it / G::STAGES) & 1u))) break;
+          if (!(ok = wait_pv_idle(0))) break;
+          tc_fence_after();
+          issue_s(0, it % G::STAGES);
+          mma_commit(bar(G::B_S_FULL + 0));
+          if (ui.t1) {
+            if (!(ok = wait_pv_idle(1))) break;
+            tc_fence_after();
+            issue_s(1, it % G::STAGES);
+            mma_commit(bar(G::B_S_FULL + 1));
+          }
+          mma_commit(bar(G::B_KV_EMPTY + it % G::STAGES));
+          if (ui.nkv == 1) mma_commit(bar(G::B_Q_EMPTY));
+          issued = true;
+        }
+        for (int j = 0; ok && j < ui.nkv; ++j) {
+          const uint32_t itv = kv_item + 2 * j + 1;
+          const uint32_t itk = itv + 1;
+          const bool more = j + 1 < ui.nkv;
+          if (!(ok = wait_(bar(G::B_KV_FULL + itv % G::STAGES), (itv / G::STAGES) & 1u))) break;
+          // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
+          if (!(ok = wait_(bar(G::B_P_FULL + 0), p_wait[0] & 1u))) break;
+          ++p_wait[0];
+          tc_fence_after();
+          issue_pv(0, itv % G::STAGES, j > 0);
+          mma_commit(bar(G::B_PV_DONE + 0));
+          ++pv_cnt[0];
+          if (more) {
+            if (!(ok = wait_(bar(G::B_KV_FULL + itk % G::STAGES), (itk / G::STAGES) & 1u))) break;
+            if (!(ok = wait_pv_idle(0))) break;
+            tc_fence_after();
+            issue_s(0, itk % G::STAGES);
+            mma_commit(bar(G::B_S_FULL + 0));
+          }
+          // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
+          if (ui.t1) {
+            if (!(ok = wait_(bar(G::B_P_FULL + 1), p_wait[1] & 1u))) break;
+            ++p_wait[1];
+            tc_fence_after();
+            issue_pv(1, itv % G::STAGES, j > 0);
+            mma_commit(bar(G::B_PV_DONE + 1));
+            ++pv_cnt[1];
+          }
+          mma_commit(bar(G::B_KV_EMPTY + itv % G::STAGES));
+          if (more) {
+            if (ui.t1) {
+              if (!(ok = wait_pv_idle(1))) break;
+              tc_fence_after();
+              issue_s(1, itk % G::STAGES);
+              mma_commit(bar(G::B_S_FULL + 1));
+            }
+            mma_commit(bar(G::B_KV_EMPTY + itk % G::STAGES));
+            if (j + 2 == ui.nkv) mma_commit(bar(G::B_Q_EMPTY));
+          }
+        }
+        kv_item += 2u * (uint32_t)ui.nkv;
+      }
+      if (issued) {
+        // every MMA this thread issued must be finished before TMEM is freed
+        mma_commit(bar(G::B_DRAIN));
+        wait_drain(bar(G::B_DRAIN), 0);
+      }
+    }
+  } else {
+    // --------------------------------------------------------- softmax
+    const int t = warp >> 2;                       // Q tile of this warpgroup
+    const int r = threadIdx.x & 127;               // row in the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + G::S_COL0 + 128u * t;
+    const uint32_t tO = tmem + lane_off + G::O_COL0 + 128u * t;
+    const float sl2 = p.scale_log2;
+    uint32_t s_wait = 0, p_cnt = 0;
+    bool ok = true;
+
+    auto wait_ = [&](uint32_t b, uint32_t parity) -> bool {
+      bool w = wait_bounded(b, parity, abort_flag, p.status, kStatusTimeoutSoftmax);
+      return __all_sync(0xffffffffu, w);
+    };
+
+    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+      const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k);
+      if (t == 1 && !ui.t1) continue;
+      const int row = ui.q0 + kBlockM * t + r;
+      const bool valid = row < ui.lq;
+      uint16_t* orow = p.out + ((size_t)(ui.qbase + row) * p.num_heads + ui.head) * D;
+      if (ui.nkv == 0) {
+        if (valid) {
+          uint4* o4 = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int c = 0; c < D * 2 / 16; ++c) o4[c] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      float m = 0.f, l = 0.f;
+      for (int j = 0; j < ui.nkv; ++j) {
+        if (!(ok = wait_(bar(G::B_S_FULL + t), s_wait & 1u))) break;
+        ++s_wait;
+        tc_fence_after();
+        uint32_t s[128];
+        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+        tmem_wait_ld();
+        float x[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(s[c]);
+        if (j == ui.nkv - 1) {
+          const int lim = ui.lk - j * kBlockN;  // valid keys in the last tile
+          if (lim < kBlockN) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c >= lim) x[c] = -INFINITY;
+          }
+        }
+        float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+#pragma unroll
+        for (int c = 4; c < 128; c += 4) {
+          mx0 = fmaxf(mx0, x[c]);
+          mx1 = fmaxf(mx1, x[c + 1]);
+          mx2 = fmaxf(mx2, x[c + 2]);
+          mx3 = fmaxf(mx3, x[c + 3]);
+        }
+        const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        if (j == 0) {
+          m = mxs;
+        } else {
+          const bool need = mxs > m + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            // O_t must hold P(j-1) V(j-1) before it is rescaled
+            if (!(ok = wait_(bar(G::B_PV_DONE + t), (p_cnt - 1) & 1u))) break;
+            tc_fence_after();
+            const float alpha = need ? ex2(m - mxs) : 1.0f;
+            if (need) m = mxs;
+            l *= alpha;
+#pragma unroll
+            for (int c = 0; c < G::DP; c += 16) {
+              uint32_t o[16];
+              tmem_ld16(tO + c, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st16(tO + c, o);
+            }
+            tmem_wait_st();
+          }
+        }
+        const float nm = -m;
+        float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = ex2(fmaf(x[2 * c], sl2, nm));
+          const float p1 = ex2(fmaf(x[2 * c + 1], sl2, nm));
+          const float p2 = ex2(fmaf(x[2 * c + 2], sl2, nm));
+          const float p3 = ex2(fmaf(x[2 * c + 3], sl2, nm));
+          sum0 += p0;
+          sum1 += p1;
+          sum2 += p2;
+          sum3 += p3;
+          pk[c] = pack_bf16x2(p0, p1);
+          pk[c + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st32(tS + 0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        tmem_wait_st();
+        l += (sum0 + sum1) + (sum2 + sum3);
+        tc_fence_before();
+        mbar_arrive(bar(G::B_P_FULL + t));
+        ++p_cnt;
+      }
+      if (!ok) break;
+      // epilogue: O / l -> bf16 -> out (rows of this sequence only)
+      if (!(ok = wait_(bar(G::B_PV_DONE + t), (p_cnt - 1) & 1u))) break;
+      tc_fence_after();
+      const float inv = 1.0f / l;
+#pragma unroll
+      for (int c = 0; c < G::DP; c += 16) {
+        uint32_t o[16];
+        tmem_ld16(tO + c, o);
+        tmem_wait_ld();
+        if (valid && c < D) {
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+          uint4* o4 = reinterpret_cast<uint4*>(orow + c);
+          o4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          if (c + 8 < D) o4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- launch
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
+  attn_varlen_plan_kernel<<<1, 1024, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_fwd_t(const FwdParams& p, int grid, cudaStream_t stream) {
+  attn_varlen_fwd_kernel<D><<<grid, kThreads, Geometry<D>::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t prepare_fwd(int head_dim) {
+  if (head_dim == 72)
+    return cudaFuncSetAttribute(attn_varlen_fwd_kernel<72>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Geometry<72>::SMEM_BYTES);
+  if (head_dim == 128)
+    return cudaFuncSetAttribute(attn_varlen_fwd_kernel<128>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Geometry<128>::SMEM_BYTES);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd(int head_dim, const FwdParams& p, int grid, cudaStream_t stream) {
+  if (head_dim == 72) return launch_fwd_t<72>(p, grid, stream);
+  if (head_dim == 128) return launch_fwd_t<128>(p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+int fwd_threads() { return kThreads; }
+
+size_t fwd_smem_bytes(int head_dim) {
+  return head_dim == 72 ? Geometry<72>::SMEM_BYTES : Geometry<128>::SMEM_BYTES;
+}
+
+int box_cols(int head_dim) { return head_dim == 72 ? Cfg<72>::BW : Cfg<128>::BW; }
+
+bool box_swizzle_128(int head_dim) { return head_dim != 72; }
+
+}  // namespace avp
