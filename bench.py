@@ -21,6 +21,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -29,7 +30,7 @@ if ROOT not in sys.path:
 
 import numpy as np  # noqa: E402
 
-from workloads import C1, C2, C3, C4, C5, make_inputs, sample_rows  # noqa: E402
+from workloads import C1, C2, C3, C4, C5, CONFIGS, make_inputs, sample_rows  # noqa: E402
 
 HEADLINE = C2
 METRIC = "varlen attn fwd TFLOP/s (4*sum(L^2)*H*D)"
@@ -59,11 +60,10 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"attn_varlen_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
@@ -134,25 +134,31 @@ def cpu_oracle_rate(w, max_seconds=12.0, nthreads=0):
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the CPU oracle, timed on the host cores."""
+    """The reference arm: the CPU oracle, timed on the host cores.
+
+    Each step is a bounded sample of the headline workload (rows of it, all
+    keys each), sized so that warm-up plus timed steps take about a minute."""
     if rank != 0:
         return
     w = HEADLINE
-    r = cpu_oracle_rate(w, max_seconds=max(2.0, 20.0 / max(args.steps, 1)))
-    ms_per_step = None
-    vals = []
-    for _ in range(args.steps):
-        vals.append(cpu_oracle_rate(w, max_seconds=max(1.0, 20.0 / max(args.steps, 1)))["tflops"])
-    val = statistics.median(vals) if vals else r["tflops"]
+    per_step = min(5.0, max(0.2, 60.0 / max(args.steps + args.warmup, 1)))
+    for _ in range(args.warmup):
+        cpu_oracle_rate(w, max_seconds=per_step)
+    runs = [cpu_oracle_rate(w, max_seconds=per_step) for _ in range(args.steps)]
+    flops = sum(r["tflops"] * r["seconds"] for r in runs)
+    secs = sum(r["seconds"] for r in runs)
+    val = flops / secs if secs > 0 else 0.0
+    rows = sum(r["rows"] for r in runs)
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "seq_lens": list(w.seq_lens_q), "num_heads": w.num_heads,
-                       "head_dim": w.head_dim},
-            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
-                             "sample": f"seeded rows of {w.name} (all keys per row), about "
-                                       f"{max(1.0, 20.0 / max(args.steps, 1)):.0f} s per step"},
+            "ms_per_step": secs / max(args.steps, 1) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "seq_lens": list(w.seq_lens_q),
+                       "num_heads": w.num_heads, "head_dim": w.head_dim},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": runs[0]["cores"] if runs else None,
+                             "kind": "oracle",
+                             "sample": f"{rows} seeded (token, head) rows of {w.name}, all keys "
+                                       f"each, {per_step:.1f} s per step"},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -191,7 +197,7 @@ def run_ours(args, rank, world, local_rank):
         return x, t, torch.from_numpy(x["cu_q"]).to(dev), torch.from_numpy(x["cu_k"]).to(dev)
 
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    w = HEADLINE
+    w = CONFIGS[args.workload] if args.workload else HEADLINE
     x, t, cu_q, cu_k = device_inputs(w)
     out = torch.empty_like(t["q"])
     step = lambda: vlp.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, out=out)  # noqa: E731
@@ -205,6 +211,12 @@ def run_ours(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clocks:
         durs = time_calls(step, args.steps, flush, stream)
     vlp.check()
+    if args.profile:
+        # kernels only (for profiler runs): no end-to-end leg, shapes or CPU baseline
+        if rank == 0:
+            print(json.dumps({"profile": True, "workload": w.name, "steps": args.steps,
+                              "ms_per_step": sum(durs) / args.steps}), flush=True)
+        return
     t_sum = sum(durs) / 1e3  # seconds of device time over the K steps
     if world > 1:
         tt = torch.tensor([t_sum], dtype=torch.float64, device=dev)
@@ -297,6 +309,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--workload", choices=sorted(CONFIGS), default=None,
+                    help="time this workload instead of the headline one")
+    ap.add_argument("--profile", action="store_true",
+                    help="warm-up and timed steps only, for runs under a profiler")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

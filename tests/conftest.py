@@ -29,3 +29,18 @@ def cuda_lib():
     import variable_length_prefill_gb300 as vlp
     vlp.load()
     return vlp
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write the parity errors of this run to $ATTN_VARLEN_REPORT_DIR, if set."""
+    try:
+        from gpu_helpers import REPORT
+    except Exception:
+        return
+    out = os.environ.get("ATTN_VARLEN_REPORT_DIR")
+    if not REPORT or not out or not os.path.isdir(out):
+        return
+    with open(os.path.join(out, "parity_report.txt"), "w") as f:
+        f.write("case elements max_abs_err mean_abs_err\n")
+        for what, n, mx, mean in REPORT:
+            f.write(f"{what} {n} {mx:.3e} {mean:.3e}\n")

@@ -104,14 +104,14 @@ def test_many_short_sequences(cuda_lib):
     the unit search over many sequences."""
     rng = np.random.default_rng(43)
     lens = tuple(int(v) for v in rng.integers(0, 5, 300)) + (1500,)
-    check_full(cuda_lib, Workload("many_short", lens, 2, 72, seed=44))
+    check_full(cuda_lib, Workload("many_short", lens, 2, 72, seed=44), short_sequences=True)
 
 
 def test_more_sequences_than_sorted_limit(cuda_lib):
     """Beyond the longest-first limit the natural order is used."""
     rng = np.random.default_rng(45)
     lens = tuple(int(v) for v in rng.integers(0, 4, 2500))
-    check_full(cuda_lib, Workload("very_many", lens, 1, 128, seed=46))
+    check_full(cuda_lib, Workload("very_many", lens, 1, 128, seed=46), short_sequences=True)
 
 
 def test_caller_workspace_on_two_streams(cuda_lib):

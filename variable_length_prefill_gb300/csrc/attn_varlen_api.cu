@@ -79,34 +79,55 @@ int check_args(const void* q, const void* k, const void* v, const int32_t* cu_q,
   return ATTN_VARLEN_OK;
 }
 
-// Host-encoded template: a 3-D bf16 map {head_dim, num_heads, rows} with box
-// {box, 1, 128}; the plan kernel patches the address and the row extent per
-// sequence.
-int encode_template(CUtensorMap* m, const void* base, int num_heads, int head_dim) {
-  const int box = avp::box_cols(head_dim);
-  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads, (cuuint64_t)avp::kBlockM};
+}  // namespace
+
+namespace avp {
+
+int encode_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int num_heads, int head_dim,
+               uint64_t rows) {
+  const int box = box_cols(head_dim);
+  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_heads * head_dim * 2};
-  cuuint32_t boxdim[3] = {(cuuint32_t)box, 1, (cuuint32_t)avp::kBlockM};
+  cuuint32_t boxdim[3] = {(cuuint32_t)box, 1, (cuuint32_t)kBlockM};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapSwizzle swz =
-      avp::box_swizzle_128(head_dim) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B;
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                        strides, boxdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? ATTN_VARLEN_OK : ATTN_VARLEN_ERR_DRIVER;
+      box_swizzle_128(head_dim) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B;
+  return (int)enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  boxdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
+
+// Templates: a 3-D bf16 map {head_dim, num_heads, rows} with box {box, 1,
+// 128}; the plan kernel patches the address and the row extent per sequence.
+// Class 0 is encoded one row short of kMapLargeBytes, class 1 at it.
+int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[kMapsPerSeq],
+                     int num_heads, int head_dim) {
+  const uint64_t row_bytes = (uint64_t)num_heads * head_dim * 2;
+  const uint64_t large_rows = (kMapLargeBytes + row_bytes - 1) / row_bytes;
+  const uint64_t small_rows = large_rows > 1 ? large_rows - 1 : 1;
+  for (int m = 0; m < kMapsPerSeq; ++m) {
+    int r = encode_map(enc, &pp.tmpl[0][m], bases[m], num_heads, head_dim, small_rows);
+    if (r) return r;
+    r = encode_map(enc, &pp.tmpl[1][m], bases[m], num_heads, head_dim, large_rows);
+    if (r) return r;
+  }
+  return 0;
+}
+
+}  // namespace avp
+
+namespace {
 
 int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const int32_t* cu_k,
         int num_seqs, int num_heads, int head_dim, void* out, void* ws, int dev,
         DeviceState& st, cudaStream_t stream) {
   avp::PlanParams pp;
   std::memset(&pp, 0, sizeof(pp));
-  const void* bases[3] = {q, k, v};
-  for (int m = 0; m < avp::kMapsPerSeq; ++m) {
-    int rc = encode_template(&pp.tmpl[m], bases[m], num_heads, head_dim);
-    if (rc) return rc;
-    pp.base[m] = static_cast<const uint8_t*>(bases[m]);
-  }
+  const void* bases[avp::kMapsPerSeq] = {q, k, v};
+  if (avp::encode_templates(reinterpret_cast<avp::EncodeTiledFn>(g_encode), pp, bases, num_heads,
+                            head_dim) != 0)
+    return ATTN_VARLEN_ERR_DRIVER;
+  for (int m = 0; m < avp::kMapsPerSeq; ++m) pp.base[m] = static_cast<const uint8_t*>(bases[m]);
   pp.cu_q = cu_q;
   pp.cu_k = cu_k;
   pp.ws = static_cast<uint8_t*>(ws);

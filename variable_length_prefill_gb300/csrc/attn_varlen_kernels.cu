@@ -13,7 +13,9 @@
 //     in that order, and writes one q, one k and one v tensor map per
 //     sequence by patching host-encoded templates (global address = the
 //     sequence's first row, row extent = the sequence length) so that TMA
-//     zero-fills every row past the end of a sequence.
+//     zero-fills every row past the end of a sequence.  The template is
+//     chosen by the sequence's byte size (see kMapLargeBytes), which makes
+//     each patched map identical to the one the host encoder would produce.
 //
 //  2. fwd (persistent, one CTA per SM, 10 warps): each CTA walks the unit
 //     list with a stride of gridDim.x.  Warp roles:
@@ -187,12 +189,13 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
     if (live && lk > 0) {
       for (int m = 0; m < kMapsPerSeq; ++m) {
         uint8_t* dst = p.ws + L.maps + ((size_t)i * kMapsPerSeq + m) * kMapBytes;
-        const uint4* src = reinterpret_cast<const uint4*>(&p.tmpl[m]);
+        const int row0 = (m == 0) ? q0 : k0;
+        const int len = (m == 0) ? lq : lk;
+        const int cls = (uint64_t)len * (uint64_t)p.row_bytes >= kMapLargeBytes ? 1 : 0;
+        const uint4* src = reinterpret_cast<const uint4*>(&p.tmpl[cls][m]);
         uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
         for (int w = 0; w < kMapBytes / 16; ++w) d4[w] = src[w];
-        const int row0 = (m == 0) ? q0 : k0;
-        const int len = (m == 0) ? lq : lk;
         tmap_set_address(dst, p.base[m] + (size_t)row0 * p.row_bytes);
         tmap_set_dim2(dst, (uint32_t)len);
       }
