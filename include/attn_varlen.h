@@ -52,6 +52,7 @@ extern "C" {
 #define ATTN_VARLEN_ERR_DEVICE_TIMEOUT    -7  /* a kernel wait ran out of time      */
 #define ATTN_VARLEN_ERR_WORKSPACE_SMALL   -8  /* caller workspace below the minimum */
 #define ATTN_VARLEN_ERR_DRIVER            -9  /* tensor-map encoder unavailable     */
+#define ATTN_VARLEN_ERR_NOALLOC_LIMIT    -10  /* num_seqs above the fixed scratch   */
 
 /*
  * attn_varlen_fwd -- the attention forward described above.
@@ -112,6 +113,36 @@ int attn_varlen_check(cudaStream_t stream);
 
 /* attn_varlen_check for a caller-owned workspace. */
 int attn_varlen_check_ws(void* workspace, cudaStream_t stream);
+
+/*
+ * attn_varlen_fwd_noalloc -- attn_varlen_fwd without any device allocation.
+ *
+ * The paper has no counterpart to this call; it exists for callers that
+ * cannot allocate device memory when they run attention: a serving process
+ * that fixes its whole memory footprint at start-up, a host framework that
+ * owns every allocation a plug-in makes, or a latency-critical path where
+ * cudaMalloc/cudaFree would synchronise the device.  Instead of the
+ * library-owned workspace, it uses one scratch array compiled into the
+ * library (about 393 KiB, held on every GPU that loads the library until
+ * the process exits), so it supports at most
+ * ATTN_VARLEN_NOALLOC_MAX_SEQS sequences per call and returns
+ * ATTN_VARLEN_ERR_NOALLOC_LIMIT above that.  Arguments, layout and results
+ * are those of attn_varlen_fwd; the call never calls cudaMalloc, cudaFree
+ * or any allocating routine.
+ *
+ * The first call on a device looks up the scratch array's device address
+ * (once, with that device current); make that first call before any stream
+ * capture.  Every call on a device shares the one array: calls that can
+ * overlap on the GPU (different streams without ordering) race and give
+ * wrong results, so order them.  Each call clears the array's status word
+ * on `stream`; device-side wait timeouts of this variant are not reported
+ * by attn_varlen_check.
+ */
+#define ATTN_VARLEN_NOALLOC_MAX_SEQS 1024
+int attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int num_seqs, int num_heads, int head_dim, void* out,
+                            cudaStream_t stream);
 
 /* Static, human-readable text for an ATTN_VARLEN_* code. */
 const char* attn_varlen_strerror(int code);

@@ -38,9 +38,12 @@ def test_return_codes_match_header():
     codes = _codes()
     assert codes["OK"] == B.OK
     for name in ("INVALID_ARG", "UNSUPPORTED_DIM", "MISALIGNED", "UNSUPPORTED_DEVICE",
-                 "CUDA", "OOM", "DEVICE_TIMEOUT", "WORKSPACE_SMALL", "DRIVER"):
+                 "CUDA", "OOM", "DEVICE_TIMEOUT", "WORKSPACE_SMALL", "DRIVER", "NOALLOC_LIMIT"):
         assert codes["ERR_" + name] == getattr(B, "ERR_" + name)
-    for c in codes.values():
+    for name, c in codes.items():
+        if name == "NOALLOC_MAX_SEQS":
+            assert c == B.NOALLOC_MAX_SEQS
+            continue
         assert vlp.strerror(c) != "unknown error code"
     assert vlp.strerror(12345) == "unknown error code"
 

@@ -6,9 +6,10 @@ non-causal, bf16 in and out.  It runs in a hand-written sm_103a CUDA library
 (TMA, tcgen05 MMA into TMEM, warp-specialised online softmax) behind the C
 ABI in include/attn_varlen.h; this package is a thin ctypes binding.
 """
-from ._binding import (AttnVarlenError, SYMBOLS, attn_varlen_fwd, check, load,
-                       strerror, workspace_size)
+from ._binding import (AttnVarlenError, SYMBOLS, attn_varlen_fwd, attn_varlen_fwd_noalloc,
+                       check, load, strerror, workspace_size)
 from .build import build, lib_path
 
-__all__ = ["AttnVarlenError", "SYMBOLS", "attn_varlen_fwd", "build", "check",
+__all__ = ["AttnVarlenError", "SYMBOLS", "attn_varlen_fwd", "attn_varlen_fwd_noalloc", "build",
+           "check",
            "lib_path", "load", "strerror", "workspace_size"]

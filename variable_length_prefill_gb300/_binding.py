@@ -22,6 +22,8 @@ ERR_OOM = -6
 ERR_DEVICE_TIMEOUT = -7
 ERR_WORKSPACE_SMALL = -8
 ERR_DRIVER = -9
+ERR_NOALLOC_LIMIT = -10
+NOALLOC_MAX_SEQS = 1024
 
 # Every symbol the header declares, with (restype, argtypes).
 _P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -33,6 +35,7 @@ SYMBOLS = {
     "attn_varlen_check_ws": (_I, [_P, _P]),
     "attn_varlen_strerror": (ctypes.c_char_p, [_I]),
     "attn_varlen_version": (_I, []),
+    "attn_varlen_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
 }
 
 _LOCK = threading.Lock()
@@ -144,3 +147,24 @@ def check(stream=None, device=None, workspace=None) -> int:
     if rc != OK:
         raise AttnVarlenError(rc, "attn_varlen_check")
     return rc
+
+
+def attn_varlen_fwd_noalloc(q, k, v, cu_seqlens_q, cu_seqlens_k, out, stream=None):
+    """attn_varlen_fwd through the entry point that allocates nothing.
+
+    For callers that must not allocate device memory at call time; ``out``
+    must be given.  Uses the library's fixed scratch (at most
+    NOALLOC_MAX_SEQS sequences per call); calls on one device must not
+    overlap on the GPU.
+    """
+    import torch
+    _check_inputs(q, k, v, cu_seqlens_q, cu_seqlens_k, out)
+    num_seqs = cu_seqlens_q.numel() - 1
+    s = _stream_handle(stream, q.device)
+    with torch.cuda.device(q.device):
+        rc = load().attn_varlen_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+                                            num_seqs, q.shape[1], q.shape[2], out.data_ptr(), s)
+    if rc != OK:
+        raise AttnVarlenError(rc, "attn_varlen_fwd_noalloc")
+    return out

@@ -29,6 +29,14 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+
+// Fixed scratch of attn_varlen_fwd_noalloc: the workspace of
+// ATTN_VARLEN_NOALLOC_MAX_SEQS sequences.  In host code the name stands for
+// the symbol, not a device address; each device's address comes from
+// cudaGetSymbolAddress (g_noalloc_ptr).
+constexpr size_t kNoAllocBytes = avp::ws_layout(ATTN_VARLEN_NOALLOC_MAX_SEQS).total;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+void* g_noalloc_ptr[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_encode_probed = false;
 
@@ -250,6 +258,36 @@ int attn_varlen_fwd_ws(const void* q, const void* k, const void* v, const int32_
              dev, st, stream);
 }
 
+int attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int num_seqs, int num_heads, int head_dim, void* out,
+                            cudaStream_t stream) {
+  int rc = check_args(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out);
+  if (rc || num_seqs == 0) return rc;
+  if (num_seqs > ATTN_VARLEN_NOALLOC_MAX_SEQS) return ATTN_VARLEN_ERR_NOALLOC_LIMIT;
+  int dev = 0;
+  if ((rc = current_device(&dev))) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if ((rc = probe_device(dev, st))) return rc;
+  if ((rc = get_encoder())) return rc;
+  if (!g_noalloc_ptr[dev]) {
+    // once per device, with `dev` current: the device address of the scratch
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return ATTN_VARLEN_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = ptr;
+  }
+  void* ws = g_noalloc_ptr[dev];
+  // the status word is the only part that must start at zero; the plan
+  // kernel rewrites everything else the attention kernel reads
+  if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return ATTN_VARLEN_ERR_CUDA;
+  return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, ws, dev,
+             st, stream);
+}
+
 int attn_varlen_check(cudaStream_t stream) {
   int dev = 0;
   int rc = current_device(&dev);
@@ -280,6 +318,9 @@ const char* attn_varlen_strerror(int code) {
     case ATTN_VARLEN_ERR_DEVICE_TIMEOUT: return "a kernel wait ran out of time";
     case ATTN_VARLEN_ERR_WORKSPACE_SMALL: return "workspace smaller than attn_varlen_workspace_size()";
     case ATTN_VARLEN_ERR_DRIVER: return "cuTensorMapEncodeTiled unavailable or failed";
+    case ATTN_VARLEN_ERR_NOALLOC_LIMIT:
+      return "num_seqs exceeds ATTN_VARLEN_NOALLOC_MAX_SEQS (1024), the fixed scratch of "
+             "attn_varlen_fwd_noalloc";
     default: return "unknown error code";
   }
 }

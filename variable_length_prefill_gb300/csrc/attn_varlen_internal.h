@@ -32,9 +32,9 @@ struct WsLayout {
   size_t total;
 };
 
-__host__ __device__ inline WsLayout ws_layout(int num_seqs) {
+__host__ __device__ constexpr WsLayout ws_layout(int num_seqs) {
   const size_t n = num_seqs > 0 ? (size_t)num_seqs : 0;
-  WsLayout w;
+  WsLayout w{};
   w.maps = 256;
   w.order = ((w.maps + n * kMapsPerSeq * kMapBytes + 255) / 256) * 256;
   w.prefix = w.order + ((n * 4 + 255) / 256) * 256;
