@@ -60,6 +60,14 @@ constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
+// S(j+1) of a tile overwrites the TMEM columns that P(j) of the same tile
+// occupies.  tcgen05.mma operations issued by one thread execute in issue
+// order, so S(j+1) is queued right behind P(j).V(j); with kStrictPvWait the
+// MMA warp instead waits for P(j).V(j) to complete before issuing S(j+1).
+#ifndef ATTN_VARLEN_STRICT_PV_WAIT
+#define ATTN_VARLEN_STRICT_PV_WAIT 0
+#endif
+constexpr bool kStrictPvWait = ATTN_VARLEN_STRICT_PV_WAIT != 0;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 
 template <int D>
@@ -404,8 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
         }
       };
       // S_t overwrites P_t: the P.V MMA that reads P_t must be finished
+      // (issue order guarantees it unless kStrictPvWait asks for the wait)
       auto wait_pv_idle = [&](int t) -> bool {
-        if (pv_cnt[t] == 0) return true;
+        if (!kStrictPvWait || pv_cnt[t] == 0) return true;
         if (!wait_(bar(G::B_PV_DONE + t), (pv_cnt[t] - 1) & 1u)) return false;
         return true;
       };
@@ -419,12 +428,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
         {
           const uint32_t it = kv_item;
           if (!(ok = wait_(bar(G::B_KV_FULL + it % G::STAGES), (it / G::STAGES) & 1u))) break;
-          if (!(ok = wait_pv_idle(0))) break;
+          ok = wait_pv_idle(0);
+          if (!ok) break;
           tc_fence_after();
           issue_s(0, it % G::STAGES);
           mma_commit(bar(G::B_S_FULL + 0));
           if (ui.t1) {
-            if (!(ok = wait_pv_idle(1))) break;
+            ok = wait_pv_idle(1);
+          if (!ok) break;
             tc_fence_after();
             issue_s(1, it % G::STAGES);
             mma_commit(bar(G::B_S_FULL + 1));
@@ -447,7 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
           ++pv_cnt[0];
           if (more) {
             if (!(ok = wait_(bar(G::B_KV_FULL + itk % G::STAGES), (itk / G::STAGES) & 1u))) break;
-            if (!(ok = wait_pv_idle(0))) break;
+            ok = wait_pv_idle(0);
+          if (!ok) break;
             tc_fence_after();
             issue_s(0, itk % G::STAGES);
             mma_commit(bar(G::B_S_FULL + 0));
@@ -464,7 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
           mma_commit(bar(G::B_KV_EMPTY + itv % G::STAGES));
           if (more) {
             if (ui.t1) {
-              if (!(ok = wait_pv_idle(1))) break;
+              ok = wait_pv_idle(1);
+          if (!ok) break;
               tc_fence_after();
               issue_s(1, itk % G::STAGES);
               mma_commit(bar(G::B_S_FULL + 1));
@@ -517,31 +530,54 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
         ++s_wait;
         tc_fence_after();
         uint32_t s[128];
+        // keys past the end of the sequence in its last tile
+        const int lim = ui.lk - j * kBlockN;
+        const bool tail = (j == ui.nkv - 1) && lim < kBlockN;
         tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        tmem_wait_ld();
+        reg_fence(s, 0, 64);
         tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
         tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-        tmem_wait_ld();
-        float x[128];
+        float mx0, mx1, mx2, mx3;
+        if (!tail) {
+          // row max of the first half while the second half is in flight
+          mx0 = __uint_as_float(s[0]);
+          mx1 = __uint_as_float(s[1]);
+          mx2 = __uint_as_float(s[2]);
+          mx3 = __uint_as_float(s[3]);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(s[c]);
-        if (j == ui.nkv - 1) {
-          const int lim = ui.lk - j * kBlockN;  // valid keys in the last tile
-          if (lim < kBlockN) {
+          for (int c = 4; c < 64; c += 8) {
+            mx0 = fmax3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+            mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+            mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+          }
+          tmem_wait_ld();
+          reg_fence(s, 64, 64);
+        } else {
+          tmem_wait_ld();
+          reg_fence(s, 64, 64);
 #pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (c >= lim) x[c] = -INFINITY;
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) s[c] = __float_as_uint(-INFINITY);
+          mx0 = mx1 = mx2 = mx3 = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            mx0 = fmax3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+            mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+            mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
           }
         }
-        float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
-        for (int c = 4; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, x[c]);
-          mx1 = fmaxf(mx1, x[c + 1]);
-          mx2 = fmaxf(mx2, x[c + 2]);
-          mx3 = fmaxf(mx3, x[c + 3]);
+        for (int c = 64; c < 128; c += 8) {
+          mx0 = fmax3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+          mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+          mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
         }
-        const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const float mxs = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
         if (j == 0) {
           m = mxs;
         } else {
@@ -558,6 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
               uint32_t o[16];
               tmem_ld16(tO + c, o);
               tmem_wait_ld();
+              reg_fence(o, 0, 16);
 #pragma unroll
               for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
               tmem_st16(tO + c, o);
@@ -565,26 +602,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
             tmem_wait_st();
           }
         }
-        const float nm = -m;
-        float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+        // p = 2^(s * scale * log2(e) - m), packed two lanes per FMA/add
+        const float2 c2 = make_float2(sl2, sl2);
+        const float2 nm2 = make_float2(-m, -m);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
         uint32_t pk[64];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float p0 = ex2(fmaf(x[2 * c], sl2, nm));
-          const float p1 = ex2(fmaf(x[2 * c + 1], sl2, nm));
-          const float p2 = ex2(fmaf(x[2 * c + 2], sl2, nm));
-          const float p3 = ex2(fmaf(x[2 * c + 3], sl2, nm));
-          sum0 += p0;
-          sum1 += p1;
-          sum2 += p2;
-          sum3 += p3;
-          pk[c] = pack_bf16x2(p0, p1);
-          pk[c + 1] = pack_bf16x2(p2, p3);
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int c = 32 * h; c < 32 * h + 32; c += 2) {
+            float2 a = __ffma2_rn(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])),
+                                  c2, nm2);
+            float2 b = __ffma2_rn(make_float2(__uint_as_float(s[2 * c + 2]),
+                                              __uint_as_float(s[2 * c + 3])), c2, nm2);
+            a.x = ex2(a.x);
+            a.y = ex2(a.y);
+            b.x = ex2(b.x);
+            b.y = ex2(b.y);
+            acc0 = __fadd2_rn(acc0, a);
+            acc1 = __fadd2_rn(acc1, b);
+            pk[c] = pack_bf16x2(a.x, a.y);
+            pk[c + 1] = pack_bf16x2(b.x, b.y);
+          }
+          tmem_st32(tS + 32 * h, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * h]));
         }
-        tmem_st32(tS + 0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
         tmem_wait_st();
-        l += (sum0 + sum1) + (sum2 + sum3);
+        l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
         tc_fence_before();
         mbar_arrive(bar(G::B_P_FULL + t));
         ++p_cnt;
@@ -599,6 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
         uint32_t o[16];
         tmem_ld16(tO + c, o);
         tmem_wait_ld();
+        reg_fence(o, 0, 16);
         if (valid && c < D) {
           uint32_t w[8];
 #pragma unroll

@@ -237,6 +237,21 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// max of three (sm_100+ three-input form)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Register fence after tcgen05.wait::ld: later uses of r depend on this point,
+// so no arithmetic on r can be scheduled before the wait.
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N], int from, int count) {
+#pragma unroll
+  for (int i = 0; i < count; ++i) asm volatile("" : "+r"(r[from + i]));
+}
+
 // bf16x2 with `lo` in the low half (round to nearest even).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
