@@ -147,6 +147,10 @@ int attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v,
 /* Static, human-readable text for an ATTN_VARLEN_* code. */
 const char* attn_varlen_strerror(int code);
 
+/* Text of the last CUDA runtime error behind an ATTN_VARLEN_ERR_CUDA return
+ * on the calling thread ("no CUDA error" if none).  Static storage. */
+const char* attn_varlen_last_cuda_error(void);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int attn_varlen_version(void);
 

@@ -36,6 +36,7 @@ SYMBOLS = {
     "attn_varlen_strerror": (ctypes.c_char_p, [_I]),
     "attn_varlen_version": (_I, []),
     "attn_varlen_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "attn_varlen_last_cuda_error": (ctypes.c_char_p, []),
 }
 
 _LOCK = threading.Lock()
@@ -45,7 +46,10 @@ _LIB = None
 class AttnVarlenError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {strerror(code)} (code {code})")
+        msg = f"{where}: {strerror(code)} (code {code})"
+        if code == ERR_CUDA:
+            msg += f": {load().attn_varlen_last_cuda_error().decode()}"
+        super().__init__(msg)
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:

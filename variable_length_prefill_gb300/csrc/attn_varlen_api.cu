@@ -40,16 +40,25 @@ void* g_noalloc_ptr[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_encode_probed = false;
 
-int map_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_VARLEN_OK : ATTN_VARLEN_ERR_CUDA; }
+// Last CUDA runtime error this library saw on the calling thread.
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+int fail_cuda(cudaError_t e) {
+  g_last_cuda_error = e;
+  cudaGetLastError();  // do not leave the error pending for the caller
+  return ATTN_VARLEN_ERR_CUDA;
+}
+
+int map_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_VARLEN_OK : fail_cuda(e); }
 
 // Called with g_mu held.
 int probe_device(int dev, DeviceState& st) {
   if (st.probed) return st.supported ? ATTN_VARLEN_OK : ATTN_VARLEN_ERR_UNSUPPORTED_DEVICE;
   int major = 0, minor = 0, sms = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return ATTN_VARLEN_ERR_CUDA;
+  cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail_cuda(e);
   st.probed = true;
   st.supported = (major == 10 && minor == 3);
   st.sm_count = sms;
@@ -155,12 +164,13 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const 
 
   const int slot = head_dim == 72 ? 0 : 1;
   if (!st.prepared[slot]) {
-    if (avp::prepare_fwd(head_dim) != cudaSuccess) return ATTN_VARLEN_ERR_CUDA;
+    cudaError_t pe = avp::prepare_fwd(head_dim);
+    if (pe != cudaSuccess) return fail_cuda(pe);
     st.prepared[slot] = true;
   }
   (void)dev;
   cudaError_t e = avp::launch_plan(pp, stream);
-  if (e != cudaSuccess) return ATTN_VARLEN_ERR_CUDA;
+  if (e != cudaSuccess) return fail_cuda(e);
   e = avp::launch_fwd(head_dim, fp, st.sm_count, stream);
   return map_cuda(e);
 }
@@ -173,9 +183,9 @@ int ensure_workspace(DeviceState& st, size_t need) {
   bytes = (bytes + 255) & ~(size_t)255;
   int status = 0;
   if (st.ws) {
-    if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_VARLEN_ERR_CUDA;
-    if (cudaMemcpy(&status, st.ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-      return ATTN_VARLEN_ERR_CUDA;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&status, st.ws, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(e);
     cudaFree(st.ws);
     st.ws = nullptr;
     st.ws_bytes = 0;
@@ -185,10 +195,11 @@ int ensure_workspace(DeviceState& st, size_t need) {
     cudaGetLastError();
     return ATTN_VARLEN_ERR_OOM;
   }
-  if (cudaMemset(p, 0, 256) != cudaSuccess ||
-      cudaMemcpy(p, &status, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+  cudaError_t e = cudaMemset(p, 0, 256);
+  if (e == cudaSuccess) e = cudaMemcpy(p, &status, sizeof(int), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
     cudaFree(p);
-    return ATTN_VARLEN_ERR_CUDA;
+    return fail_cuda(e);
   }
   st.ws = p;
   st.ws_bytes = bytes;
@@ -196,20 +207,21 @@ int ensure_workspace(DeviceState& st, size_t need) {
 }
 
 int current_device(int* dev) {
-  if (cudaGetDevice(dev) != cudaSuccess) return ATTN_VARLEN_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return fail_cuda(e);
   if (*dev < 0 || *dev >= kMaxDevices) return ATTN_VARLEN_ERR_UNSUPPORTED_DEVICE;
   return ATTN_VARLEN_OK;
 }
 
 int read_and_clear_status(void* ws, cudaStream_t stream) {
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_VARLEN_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(stream);
   int status = 0;
-  if (cudaMemcpy(&status, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return ATTN_VARLEN_ERR_CUDA;
+  if (e == cudaSuccess) e = cudaMemcpy(&status, ws, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e);
   if (status != 0) {
     const int zero = 0;
-    if (cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
-      return ATTN_VARLEN_ERR_CUDA;
+    e = cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail_cuda(e);
     return ATTN_VARLEN_ERR_DEVICE_TIMEOUT;
   }
   return ATTN_VARLEN_OK;
@@ -274,16 +286,16 @@ int attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v,
   if (!g_noalloc_ptr[dev]) {
     // once per device, with `dev` current: the device address of the scratch
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
-      cudaGetLastError();
-      return ATTN_VARLEN_ERR_CUDA;
-    }
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (!ptr) return ATTN_VARLEN_ERR_CUDA;
     g_noalloc_ptr[dev] = ptr;
   }
   void* ws = g_noalloc_ptr[dev];
   // the status word is the only part that must start at zero; the plan
   // kernel rewrites everything else the attention kernel reads
-  if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return ATTN_VARLEN_ERR_CUDA;
+  cudaError_t me = cudaMemsetAsync(ws, 0, sizeof(int), stream);
+  if (me != cudaSuccess) return fail_cuda(me);
   return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, ws, dev,
              st, stream);
 }
@@ -297,7 +309,7 @@ int attn_varlen_check(cudaStream_t stream) {
     std::lock_guard<std::mutex> lock(g_mu);
     ws = g_dev[dev].ws;
   }
-  if (!ws) return cudaStreamSynchronize(stream) == cudaSuccess ? ATTN_VARLEN_OK : ATTN_VARLEN_ERR_CUDA;
+  if (!ws) return map_cuda(cudaStreamSynchronize(stream));
   return read_and_clear_status(ws, stream);
 }
 
@@ -326,5 +338,9 @@ const char* attn_varlen_strerror(int code) {
 }
 
 int attn_varlen_version(void) { return 100; }
+
+const char* attn_varlen_last_cuda_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(g_last_cuda_error);
+}
 
 }  // extern "C"

@@ -287,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base_ptr + G::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + G::MISC_OFF + 4);
 
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  // warp index made warp-uniform for the compiler (role branches below)
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(G::B_Q_FULL), 1);
@@ -322,177 +322,187 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      uint32_t kv_item = 0, q_use = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-        const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k);
-        if (ui.nkv == 0) continue;
-        const uint8_t* mq = p.ws + L.maps + (size_t)ui.seq * kMapsPerSeq * kMapBytes;
-        const uint8_t* mk = mq + kMapBytes;
-        const uint8_t* mv = mq + 2 * kMapBytes;
+    // The whole warp runs the loop (uniform control flow); one elected lane
+    // issues each TMA and expect-tx.
+    const uint32_t leader = elect_one();
+    uint32_t kv_item = 0, q_use = 0;
+    bool ok = true;
+    auto wait_ = [&](uint32_t b, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu,
+                        wait_bounded(b, parity, abort_flag, p.status, kStatusTimeoutLoad));
+    };
+    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+      const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k);
+      if (ui.nkv == 0) continue;
+      const uint8_t* mq = p.ws + L.maps + (size_t)ui.seq * kMapsPerSeq * kMapBytes;
+      const uint8_t* mk = mq + kMapBytes;
+      const uint8_t* mv = mq + 2 * kMapBytes;
+      if (leader) {
         tmap_acquire(mq);
         tmap_acquire(mk);
         tmap_acquire(mv);
-        if (!(ok = wait_bounded(bar(G::B_Q_EMPTY), (q_use & 1u) ^ 1u, abort_flag, p.status,
-                                kStatusTimeoutLoad)))
-          break;
-        ++q_use;
-        mbar_arrive_expect_tx(bar(G::B_Q_FULL), (ui.t1 ? 2u : 1u) * G::TILE_BYTES);
+      }
+      __syncwarp();
+      if (!(ok = wait_(bar(G::B_Q_EMPTY), (q_use & 1u) ^ 1u))) break;
+      ++q_use;
+      mbar_arrive_expect_tx_if(leader, bar(G::B_Q_FULL), (ui.t1 ? 2u : 1u) * G::TILE_BYTES);
+#pragma unroll
+      for (int b = 0; b < G::NB; ++b)
+        tma_load_3d_if(leader, sQ + b * G::BOX_BYTES, mq, bar(G::B_Q_FULL), b * G::BW, ui.head,
+                       ui.q0);
+      if (ui.t1) {
 #pragma unroll
         for (int b = 0; b < G::NB; ++b)
-          tma_load_3d(sQ + b * G::BOX_BYTES, mq, bar(G::B_Q_FULL), b * G::BW, ui.head, ui.q0);
-        if (ui.t1) {
+          tma_load_3d_if(leader, sQ + G::TILE_BYTES + b * G::BOX_BYTES, mq, bar(G::B_Q_FULL),
+                         b * G::BW, ui.head, ui.q0 + kBlockM);
+      }
+      for (int j = 0; ok && j < ui.nkv; ++j) {
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t stage = kv_item % G::STAGES;
+          const uint32_t use = kv_item / G::STAGES;
+          if (!(ok = wait_(bar(G::B_KV_EMPTY + stage), (use & 1u) ^ 1u))) break;
+          mbar_arrive_expect_tx_if(leader, bar(G::B_KV_FULL + stage), G::TILE_BYTES);
+          const uint8_t* m = which ? mv : mk;
+          const uint32_t dst = sKV + stage * G::TILE_BYTES;
 #pragma unroll
           for (int b = 0; b < G::NB; ++b)
-            tma_load_3d(sQ + G::TILE_BYTES + b * G::BOX_BYTES, mq, bar(G::B_Q_FULL), b * G::BW,
-                        ui.head, ui.q0 + kBlockM);
-        }
-        for (int j = 0; ok && j < ui.nkv; ++j) {
-          for (int which = 0; which < 2; ++which) {
-            const uint32_t stage = kv_item % G::STAGES;
-            const uint32_t use = kv_item / G::STAGES;
-            if (!(ok = wait_bounded(bar(G::B_KV_EMPTY + stage), (use & 1u) ^ 1u, abort_flag,
-                                    p.status, kStatusTimeoutLoad)))
-              break;
-            mbar_arrive_expect_tx(bar(G::B_KV_FULL + stage), G::TILE_BYTES);
-            const uint8_t* m = which ? mv : mk;
-            const uint32_t dst = sKV + stage * G::TILE_BYTES;
-#pragma unroll
-            for (int b = 0; b < G::NB; ++b)
-              tma_load_3d(dst + b * G::BOX_BYTES, m, bar(G::B_KV_FULL + stage), b * G::BW,
-                          ui.head, j * kBlockN);
-            ++kv_item;
-          }
+            tma_load_3d_if(leader, dst + b * G::BOX_BYTES, m, bar(G::B_KV_FULL + stage),
+                           b * G::BW, ui.head, j * kBlockN);
+          ++kv_item;
         }
       }
-      if (!ok) {
-        // let every copy already issued land before the CTA can exit
-        if (q_use > 0) wait_drain(bar(G::B_Q_FULL), (q_use - 1) & 1u);
-        const uint32_t first = kv_item > (uint32_t)G::STAGES ? kv_item - G::STAGES : 0;
-        for (uint32_t it = first; it < kv_item; ++it)
-          wait_drain(bar(G::B_KV_FULL + it % G::STAGES), (it / G::STAGES) & 1u);
-      }
+    }
+    if (!ok) {
+      // let every copy already issued land before the CTA can exit
+      if (q_use > 0) wait_drain(bar(G::B_Q_FULL), (q_use - 1) & 1u);
+      const uint32_t first = kv_item > (uint32_t)G::STAGES ? kv_item - G::STAGES : 0;
+      for (uint32_t it = first; it < kv_item; ++it)
+        wait_drain(bar(G::B_KV_FULL + it % G::STAGES), (it / G::STAGES) & 1u);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, kBlockN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, G::DP, false, true);
-      uint32_t kv_item = 0, q_use = 0;
-      uint32_t p_wait[2] = {0, 0};  // p_full phases consumed per tile
-      uint32_t pv_cnt[2] = {0, 0};  // P.V groups committed per tile
-      bool ok = true;
-      bool issued = false;
+    // The whole warp runs the loop; descriptors are computed once per tile
+    // base and advanced by constants, and one elected lane issues each
+    // tcgen05.mma and commit (commits track that lane's MMAs).
+    const uint32_t leader = elect_one();
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, G::DP, false, true);
+    // K-major (Q, K) and MN-major (V) descriptors of the first tile of each
+    // region; a byte offset `o` inside shared memory adds o >> 4.
+    const uint64_t dq0 = smem_desc(sQ, 16, G::SBO, G::SWZ);
+    const uint64_t dk0 = smem_desc(sKV, 16, G::SBO, G::SWZ);
+    const uint64_t dv0 = smem_desc(sKV, G::BOX_BYTES, G::SBO, G::SWZ);
+    uint32_t kv_item = 0, q_use = 0;
+    uint32_t p_wait[2] = {0, 0};  // p_full phases consumed per tile
+    uint32_t pv_cnt[2] = {0, 0};  // P.V groups committed per tile
+    bool ok = true;
+    bool issued = false;
 
-      auto wait_ = [&](uint32_t b, uint32_t parity) -> bool {
-        return wait_bounded(b, parity, abort_flag, p.status, kStatusTimeoutMma);
-      };
-      // S_t = Q_t K^T : K from stage `ks`
-      auto issue_s = [&](int t, uint32_t ks) {
-        const uint32_t qa = sQ + t * G::TILE_BYTES;
-        const uint32_t kb = sKV + ks * G::TILE_BYTES;
-        const uint32_t d = tmem + G::S_COL0 + 128u * t;
+    auto wait_ = [&](uint32_t b, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu,
+                        wait_bounded(b, parity, abort_flag, p.status, kStatusTimeoutMma));
+    };
+    // S_t = Q_t K^T : K from stage `ks`
+    auto issue_s = [&](int t, uint32_t ks) {
+      const uint64_t qa = dq0 + ((t * G::TILE_BYTES) >> 4);
+      const uint64_t kb = dk0 + ((ks * G::TILE_BYTES) >> 4);
+      const uint32_t d = tmem + G::S_COL0 + 128u * t;
 #pragma unroll
-        for (int k = 0; k < G::NK_S; ++k) {
-          const uint32_t off = (k * 16 / G::BW) * G::BOX_BYTES + ((k * 16) % G::BW) * 2;
-          mma_ss(d, smem_desc(qa + off, 16, G::SBO, G::SWZ), smem_desc(kb + off, 16, G::SBO, G::SWZ),
-                 idesc_s, k > 0 ? 1u : 0u);
-        }
-      };
-      // O_t (+)= P_t V : V from stage `vs`, P from TMEM (aliasing S_t)
-      auto issue_pv = [&](int t, uint32_t vs, bool acc) {
-        const uint32_t vb = sKV + vs * G::TILE_BYTES;
-        const uint32_t d = tmem + G::O_COL0 + 128u * t;
-        const uint32_t a = tmem + G::S_COL0 + 128u * t;
+      for (int k = 0; k < G::NK_S; ++k) {
+        const uint32_t off = ((k * 16 / G::BW) * G::BOX_BYTES + ((k * 16) % G::BW) * 2) >> 4;
+        mma_ss_if(leader, d, qa + off, kb + off, idesc_s, k > 0 ? 1u : 0u);
+      }
+    };
+    // O_t (+)= P_t V : V from stage `vs`, P from TMEM (aliasing S_t)
+    auto issue_pv = [&](int t, uint32_t vs, bool acc) {
+      const uint64_t vb = dv0 + ((vs * G::TILE_BYTES) >> 4);
+      const uint32_t d = tmem + G::O_COL0 + 128u * t;
+      const uint32_t a = tmem + G::S_COL0 + 128u * t;
 #pragma unroll
-        for (int k = 0; k < G::NK_PV; ++k) {
-          const uint64_t bdesc = smem_desc(vb + k * 16 * G::BW * 2, G::BOX_BYTES, G::SBO, G::SWZ);
-          mma_ts(d, a + 8u * k, bdesc, idesc_pv, (acc || k > 0) ? 1u : 0u);
-        }
-      };
-      // S_t overwrites P_t: the P.V MMA that reads P_t must be finished
-      // (issue order guarantees it unless kStrictPvWait asks for the wait)
-      auto wait_pv_idle = [&](int t) -> bool {
-        if (!kStrictPvWait || pv_cnt[t] == 0) return true;
-        if (!wait_(bar(G::B_PV_DONE + t), (pv_cnt[t] - 1) & 1u)) return false;
-        return true;
-      };
+      for (int k = 0; k < G::NK_PV; ++k)
+        mma_ts_if(leader, d, a + 8u * k, vb + ((k * 16 * G::BW * 2) >> 4), idesc_pv,
+                  (acc || k > 0) ? 1u : 0u);
+    };
+    // S_t overwrites P_t: the P.V MMA that reads P_t must be finished
+    // (issue order guarantees it unless kStrictPvWait asks for the wait)
+    auto wait_pv_idle = [&](int t) -> bool {
+      if (!kStrictPvWait || pv_cnt[t] == 0) return true;
+      return wait_(bar(G::B_PV_DONE + t), (pv_cnt[t] - 1) & 1u);
+    };
 
-      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-        const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k);
-        if (ui.nkv == 0) continue;
-        if (!(ok = wait_(bar(G::B_Q_FULL), q_use & 1u))) break;
-        ++q_use;
-        // j = 0: S0, S1 from K_0
-        {
-          const uint32_t it = kv_item;
-          if (!(ok = wait_(bar(G::B_KV_FULL + it % G::STAGES), (it / G::STAGES) & 1u))) break;
-          ok = wait_pv_idle(0);
+    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+      const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k);
+      if (ui.nkv == 0) continue;
+      if (!(ok = wait_(bar(G::B_Q_FULL), q_use & 1u))) break;
+      ++q_use;
+      // j = 0: S0, S1 from K_0
+      {
+        const uint32_t it = kv_item;
+        if (!(ok = wait_(bar(G::B_KV_FULL + it % G::STAGES), (it / G::STAGES) & 1u))) break;
+        ok = wait_pv_idle(0);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(0, it % G::STAGES);
+        mma_commit_if(leader, bar(G::B_S_FULL + 0));
+        if (ui.t1) {
+          ok = wait_pv_idle(1);
           if (!ok) break;
           tc_fence_after();
-          issue_s(0, it % G::STAGES);
-          mma_commit(bar(G::B_S_FULL + 0));
+          issue_s(1, it % G::STAGES);
+          mma_commit_if(leader, bar(G::B_S_FULL + 1));
+        }
+        mma_commit_if(leader, bar(G::B_KV_EMPTY + it % G::STAGES));
+        if (ui.nkv == 1) mma_commit_if(leader, bar(G::B_Q_EMPTY));
+        issued = true;
+      }
+      for (int j = 0; ok && j < ui.nkv; ++j) {
+        const uint32_t itv = kv_item + 2 * j + 1;
+        const uint32_t itk = itv + 1;
+        const bool more = j + 1 < ui.nkv;
+        if (!(ok = wait_(bar(G::B_KV_FULL + itv % G::STAGES), (itv / G::STAGES) & 1u))) break;
+        // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
+        if (!(ok = wait_(bar(G::B_P_FULL + 0), p_wait[0] & 1u))) break;
+        ++p_wait[0];
+        tc_fence_after();
+        issue_pv(0, itv % G::STAGES, j > 0);
+        mma_commit_if(leader, bar(G::B_PV_DONE + 0));
+        ++pv_cnt[0];
+        if (more) {
+          if (!(ok = wait_(bar(G::B_KV_FULL + itk % G::STAGES), (itk / G::STAGES) & 1u))) break;
+          ok = wait_pv_idle(0);
+        if (!ok) break;
+          tc_fence_after();
+          issue_s(0, itk % G::STAGES);
+          mma_commit_if(leader, bar(G::B_S_FULL + 0));
+        }
+        // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
+        if (ui.t1) {
+          if (!(ok = wait_(bar(G::B_P_FULL + 1), p_wait[1] & 1u))) break;
+          ++p_wait[1];
+          tc_fence_after();
+          issue_pv(1, itv % G::STAGES, j > 0);
+          mma_commit_if(leader, bar(G::B_PV_DONE + 1));
+          ++pv_cnt[1];
+        }
+        mma_commit_if(leader, bar(G::B_KV_EMPTY + itv % G::STAGES));
+        if (more) {
           if (ui.t1) {
             ok = wait_pv_idle(1);
           if (!ok) break;
             tc_fence_after();
-            issue_s(1, it % G::STAGES);
-            mma_commit(bar(G::B_S_FULL + 1));
+            issue_s(1, itk % G::STAGES);
+            mma_commit_if(leader, bar(G::B_S_FULL + 1));
           }
-          mma_commit(bar(G::B_KV_EMPTY + it % G::STAGES));
-          if (ui.nkv == 1) mma_commit(bar(G::B_Q_EMPTY));
-          issued = true;
+          mma_commit_if(leader, bar(G::B_KV_EMPTY + itk % G::STAGES));
+          if (j + 2 == ui.nkv) mma_commit_if(leader, bar(G::B_Q_EMPTY));
         }
-        for (int j = 0; ok && j < ui.nkv; ++j) {
-          const uint32_t itv = kv_item + 2 * j + 1;
-          const uint32_t itk = itv + 1;
-          const bool more = j + 1 < ui.nkv;
-          if (!(ok = wait_(bar(G::B_KV_FULL + itv % G::STAGES), (itv / G::STAGES) & 1u))) break;
-          // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
-          if (!(ok = wait_(bar(G::B_P_FULL + 0), p_wait[0] & 1u))) break;
-          ++p_wait[0];
-          tc_fence_after();
-          issue_pv(0, itv % G::STAGES, j > 0);
-          mma_commit(bar(G::B_PV_DONE + 0));
-          ++pv_cnt[0];
-          if (more) {
-            if (!(ok = wait_(bar(G::B_KV_FULL + itk % G::STAGES), (itk / G::STAGES) & 1u))) break;
-            ok = wait_pv_idle(0);
-          if (!ok) break;
-            tc_fence_after();
-            issue_s(0, itk % G::STAGES);
-            mma_commit(bar(G::B_S_FULL + 0));
-          }
-          // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
-          if (ui.t1) {
-            if (!(ok = wait_(bar(G::B_P_FULL + 1), p_wait[1] & 1u))) break;
-            ++p_wait[1];
-            tc_fence_after();
-            issue_pv(1, itv % G::STAGES, j > 0);
-            mma_commit(bar(G::B_PV_DONE + 1));
-            ++pv_cnt[1];
-          }
-          mma_commit(bar(G::B_KV_EMPTY + itv % G::STAGES));
-          if (more) {
-            if (ui.t1) {
-              ok = wait_pv_idle(1);
-          if (!ok) break;
-              tc_fence_after();
-              issue_s(1, itk % G::STAGES);
-              mma_commit(bar(G::B_S_FULL + 1));
-            }
-            mma_commit(bar(G::B_KV_EMPTY + itk % G::STAGES));
-            if (j + 2 == ui.nkv) mma_commit(bar(G::B_Q_EMPTY));
-          }
-        }
-        kv_item += 2u * (uint32_t)ui.nkv;
       }
-      if (issued) {
-        // every MMA this thread issued must be finished before TMEM is freed
-        mma_commit(bar(G::B_DRAIN));
-        wait_drain(bar(G::B_DRAIN), 0);
-      }
+      kv_item += 2u * (uint32_t)ui.nkv;
+    }
+    if (issued) {
+      // every MMA this warp issued must be finished before TMEM is freed
+      mma_commit_if(leader, bar(G::B_DRAIN));
+      wait_drain(bar(G::B_DRAIN), 0);
     }
   } else {
     // --------------------------------------------------------- softmax
