@@ -39,6 +39,31 @@ PAGE_TPROD_TFLOPS = {  # the page's T_Prod converted with the same FLOP count
 L2_FLUSH_BYTES = 256 << 20
 
 
+def kernel_source_sha() -> str:
+    import hashlib
+    csrc = os.path.join(ROOT, "variable_length_prefill_gb300", "csrc")
+    h = hashlib.sha256()
+    for n in sorted(os.listdir(csrc)):
+        h.update(n.encode())
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload_name: str):
+    """DRAM bytes of one fwd launch from the committed ncu summary, or None
+    when the kernel sources changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("csrc_sha256") != kernel_source_sha():
+        return None
+    return d.get("traffic_bytes", {}).get(workload_name)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -286,7 +311,9 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "tensor", "achieved": round(per_call_tflops, 2),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(per_call_tflops / peaks["bf16_tflops"], 4),
-                     "traffic": None, "peak_source": peaks["source"] + " bf16 burst",
+                     "traffic": measured_traffic(w.name),
+                     "algorithmic_bytes": w.algorithmic_bytes(),
+                     "peak_source": peaks["source"] + " bf16 burst",
                      "kernel": "attn_varlen_fwd_kernel<72> (+ plan kernel in the timed call)"},
         "cpu_baseline": {"value": cpu["tflops"], "unit": "TFLOP/s", "cores": cpu["cores"],
                          "kind": "oracle", "rows_per_s": cpu["rows_per_s"],
