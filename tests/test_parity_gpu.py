@@ -114,6 +114,45 @@ def test_more_sequences_than_sorted_limit(cuda_lib):
     check_full(cuda_lib, Workload("very_many", lens, 1, 128, seed=46), short_sequences=True)
 
 
+def _scale_keys(x, scale_of_key):
+    """k rows times a per-key factor, rounded back to bf16 (test input only)."""
+    from workloads import bf16_bits_to_f64, round_to_bf16_bits
+    cu = x["cu_k"]
+    k = bf16_bits_to_f64(x["k"])
+    for i in range(len(cu) - 1):
+        for j in range(cu[i + 1] - cu[i]):
+            k[cu[i] + j] *= scale_of_key(j)
+    x["k"] = round_to_bf16_bits(k.astype(np.float32))
+    return x
+
+
+@pytest.mark.parametrize("D", [72, 128])
+def test_running_max_rises_every_tile(cuda_lib, D):
+    """Key norms step up every 128 keys, so a row's running max rises by more
+    than the rescale threshold at tile starts: the O/l rescale runs."""
+    w = Workload(f"rising_tiles_{D}", (700, 300), 2, D, seed=51)
+    x = _scale_keys(make_inputs(w), lambda j: 1.0 + 2.5 * (j // 128))
+    check_full(cuda_lib, w, x=x, short_sequences=True)
+
+
+@pytest.mark.parametrize("D", [72, 128])
+def test_running_max_rises_in_second_half(cuda_lib, D):
+    """Only the second 64 keys of each tile step up, so the first half's P is
+    computed against the old max and must be rescaled with O and l."""
+    w = Workload(f"rising_halves_{D}", (640, 200), 2, D, seed=52)
+    x = _scale_keys(make_inputs(w), lambda j: 1.0 + 3.0 * (j // 128) + (2.5 if j % 128 >= 64 else 0.0))
+    check_full(cuda_lib, w, x=x, short_sequences=True)
+
+
+@pytest.mark.parametrize("D", [72, 128])
+def test_running_max_huge_jump(cuda_lib, D):
+    """A jump far beyond the exp2 range of the old max (scores x60 from key
+    300 on): no overflow leaks into the result."""
+    w = Workload(f"huge_jump_{D}", (520,), 2, D, seed=53)
+    x = _scale_keys(make_inputs(w), lambda j: 60.0 if j >= 300 else 1.0)
+    check_full(cuda_lib, w, x=x, short_sequences=True)
+
+
 def test_caller_workspace_on_two_streams(cuda_lib):
     import torch
     x = make_inputs(C1)
