@@ -33,10 +33,12 @@
 //     rescale: the running max is only raised (and O rescaled in TMEM) when a
 //     row's new max exceeds it by more than kRescaleThreshold (log2 units).
 //
-// Head dims: 128 runs natively (two 64-column TMA boxes, 128-byte swizzle);
-// 72 is padded to 80 (five 16-column boxes, 32-byte swizzle; TMA zero-fills
-// columns 72-79 of Q and K, so they add nothing to Q.K^T, and the padded
-// output columns are never stored).  The scale always uses the true head_dim.
+// Head dims: 128 runs natively; 72 is padded to 80.  Both load every tile as
+// two 64-column TMA boxes with 128-byte swizzle; for 72 the second box holds
+// columns 64-71 and TMA zero fill, so columns 72-79 of Q and K add nothing to
+// Q.K^T, the MMAs use K = 80 and N = 80 (the first 16 columns of the second
+// box), and the padded output columns are never stored.  The scale always
+// uses the true head_dim.
 //
 // Every mbarrier wait is bounded in time; a wait that runs out records a bit
 // in the workspace status word, raises a CTA-wide abort flag, and the CTA
@@ -75,9 +77,10 @@ struct Cfg;
 template <>
 struct Cfg<72> {
   static constexpr int DP = 80;   // padded head_dim (MMA K and N multiple of 16)
-  static constexpr int BW = 16;   // columns per TMA box
-  static constexpr int STAGES = 6;
-  static constexpr uint32_t SWZ = kSwizzle32B;
+  static constexpr int BW = 64;   // columns per TMA box: two boxes, the second
+                                  // holding columns 64-71 and zero fill
+  static constexpr int STAGES = 4;
+  static constexpr uint32_t SWZ = kSwizzle128B;
 };
 template <>
 struct Cfg<128> {
@@ -91,11 +94,11 @@ template <int D>
 struct Geometry {
   static constexpr int DP = Cfg<D>::DP;
   static constexpr int BW = Cfg<D>::BW;
-  static constexpr int NB = DP / BW;                        // boxes per tile
+  static constexpr int NB = (DP + BW - 1) / BW;             // boxes per tile
   static constexpr int STAGES = Cfg<D>::STAGES;
   static constexpr uint32_t SWZ = Cfg<D>::SWZ;
   static constexpr uint32_t BOX_BYTES = kBlockM * BW * 2;   // one box: 128 rows x BW
-  static constexpr uint32_t TILE_BYTES = kBlockM * DP * 2;  // one Q/K/V tile
+  static constexpr uint32_t TILE_BYTES = NB * BOX_BYTES;    // one Q/K/V tile in smem
   static constexpr uint32_t SBO = 8 * BW * 2;               // 8-row group stride
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t KV_OFF = 2 * TILE_BYTES;
@@ -713,6 +716,8 @@ size_t fwd_smem_bytes(int head_dim) {
 
 int box_cols(int head_dim) { return head_dim == 72 ? Cfg<72>::BW : Cfg<128>::BW; }
 
-bool box_swizzle_128(int head_dim) { return head_dim != 72; }
+bool box_swizzle_128(int head_dim) {
+  return (head_dim == 72 ? Cfg<72>::SWZ : Cfg<128>::SWZ) == kSwizzle128B;
+}
 
 }  // namespace avp
