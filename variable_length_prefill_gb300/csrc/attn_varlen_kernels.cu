@@ -72,6 +72,10 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr bool kStrictPvWait = ATTN_VARLEN_STRICT_PV_WAIT != 0;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 
+#ifndef ATTN_VARLEN_KV_STAGES
+#define ATTN_VARLEN_KV_STAGES 4
+#endif
+
 template <int D>
 struct Cfg;
 template <>
@@ -79,14 +83,14 @@ struct Cfg<72> {
   static constexpr int DP = 80;   // padded head_dim (MMA K and N multiple of 16)
   static constexpr int BW = 64;   // columns per TMA box: two boxes, the second
                                   // holding columns 64-71 and zero fill
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = ATTN_VARLEN_KV_STAGES;
   static constexpr uint32_t SWZ = kSwizzle128B;
 };
 template <>
 struct Cfg<128> {
   static constexpr int DP = 128;
   static constexpr int BW = 64;
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = ATTN_VARLEN_KV_STAGES;
   static constexpr uint32_t SWZ = kSwizzle128B;
 };
 
@@ -109,6 +113,7 @@ struct Geometry {
                        B_PV_DONE = B_P_FULL + 2, B_DRAIN = B_PV_DONE + 2, NUM_BARS = B_DRAIN + 1;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // tmem slot, abort flag
   static constexpr uint32_t SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
+  static_assert(SMEM_BYTES <= 232448, "shared memory above the sm_103 per-block limit");
   static constexpr int NK_S = DP / 16;        // K-steps of S = Q K^T
   static constexpr int NK_PV = kBlockN / 16;  // K-steps of O += P V
   static constexpr uint32_t S_COL0 = 0, O_COL0 = 256;
