@@ -20,6 +20,10 @@ SMALL = [
     ((5, 130, 0, 257, 1, 64), None, 3, 72), ((5, 130, 0, 257, 1, 64), None, 3, 128),
     ((100, 300, 7), (257, 64, 1000), 2, 72), ((100, 300, 7), (257, 64, 1000), 2, 128),
     ((10, 5, 3), (0, 7, 0), 2, 72),
+    # one Q tile against many key tiles, two Q tiles against fewer key tiles
+    # than score buffers: the score/P buffer rotation must not lap a barrier
+    ((7,), (1000,), 2, 72), ((7,), (1000,), 2, 128), ((130,), (1000,), 1, 72),
+    ((300, 1, 200), (64, 2000, 30), 2, 72), ((300, 1, 200), (64, 2000, 30), 2, 128),
 ]
 
 
