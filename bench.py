@@ -188,6 +188,23 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(x: float, device) -> float:
+    """Largest value of x over all ranks (the slowest rank sets the time)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(flops_per_step: float, steps: int, world: int, seconds: float) -> float:
+    """TFLOP/s of all ranks together: every rank runs the same workload
+    (weak scaling), timed by the slowest rank."""
+    return flops_per_step * steps * world / seconds / 1e12
+
+
 def time_calls(fn, steps, flush_buf, stream):
     import torch
     durs = []
@@ -242,13 +259,9 @@ def run_ours(args, rank, world, local_rank):
             print(json.dumps({"profile": True, "workload": w.name, "steps": args.steps,
                               "ms_per_step": sum(durs) / args.steps}), flush=True)
         return
-    t_sum = sum(durs) / 1e3  # seconds of device time over the K steps
-    if world > 1:
-        tt = torch.tensor([t_sum], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_sum = float(tt.item())
+    t_sum = max_over_ranks(sum(durs) / 1e3, dev)  # seconds of device time over the K steps
     flops = w.flops()
-    value = flops * args.steps * world / t_sum / 1e12
+    value = whole_job_throughput(flops, args.steps, world, t_sum)
     ms_per_step = t_sum / args.steps * 1e3
     per_call_tflops = flops / (t_sum / args.steps) / 1e12
 
@@ -276,7 +289,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_steps = max(3, min(args.steps, 20))
     e2e_durs = time_calls(e2e_step, e2e_steps, None, stream)
-    e2e_value = flops / (sum(e2e_durs) / 1e3 / e2e_steps) / 1e12 * world
+    e2e_value = whole_job_throughput(flops, e2e_steps, world,
+                                     max_over_ranks(sum(e2e_durs) / 1e3, dev))
 
     # every workload once more: microseconds per call and TFLOP/s
     shapes = {}

@@ -1,0 +1,47 @@
+"""bench.py's multi-rank timing on CPU: two gloo ranks, the slowest rank's
+time sets the whole-job throughput (weak scaling)."""
+import os
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _rank(rank, world, port, q):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        t = bench.max_over_ranks(1.0 + rank, "cpu")
+        v = bench.whole_job_throughput(1e12, 10, world, t)
+        q.put((rank, t, v))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, t, v in res:
+        assert t == 2.0                       # max over ranks
+        assert v == pytest.approx(1e12 * 10 * 2 / 2.0 / 1e12)  # 10 TFLOP/s job-wide
+
+
+def test_single_process_needs_no_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5, "cpu") == 3.5
+    assert bench.whole_job_throughput(2e12, 4, 1, 2.0) == pytest.approx(4.0)
