@@ -24,6 +24,10 @@ SMALL = [
     # than score buffers: the score/P buffer rotation must not lap a barrier
     ((7,), (1000,), 2, 72), ((7,), (1000,), 2, 128), ((130,), (1000,), 1, 72),
     ((300, 1, 200), (64, 2000, 30), 2, 72), ((300, 1, 200), (64, 2000, 30), 2, 128),
+    # key counts on both sides of the head_dim-72 key tile (112 keys) and its
+    # multiples, with one and two Q tiles
+    ((200,), (111,), 2, 72), ((200,), (112,), 2, 72), ((129,), (113,), 2, 72),
+    ((300,), (224,), 1, 72), ((257,), (225,), 2, 72), ((112, 113, 224), None, 2, 72),
 ]
 
 

@@ -101,11 +101,11 @@ int check_args(const void* q, const void* k, const void* v, const int32_t* cu_q,
 namespace avp {
 
 int encode_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int num_heads, int head_dim,
-               uint64_t rows) {
+               uint64_t rows, int box_rows) {
   const int box = box_cols(head_dim);
   cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_heads * head_dim * 2};
-  cuuint32_t boxdim[3] = {(cuuint32_t)box, 1, (cuuint32_t)kBlockM};
+  cuuint32_t boxdim[3] = {(cuuint32_t)box, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapSwizzle swz =
       box_swizzle_128(head_dim) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B;
@@ -115,7 +115,8 @@ int encode_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int num_head
 }
 
 // Templates: a 3-D bf16 map {head_dim, num_heads, rows} with box {box, 1,
-// 128}; the plan kernel patches the address and the row extent per sequence.
+// rows per tile} (128 query rows for q, kv_tile_rows keys for k and v); the
+// plan kernel patches the address and the row extent per sequence.
 // Class 0 is encoded one row short of kMapLargeBytes, class 1 at it.
 int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[kMapsPerSeq],
                      int num_heads, int head_dim) {
@@ -123,9 +124,10 @@ int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[
   const uint64_t large_rows = (kMapLargeBytes + row_bytes - 1) / row_bytes;
   const uint64_t small_rows = large_rows > 1 ? large_rows - 1 : 1;
   for (int m = 0; m < kMapsPerSeq; ++m) {
-    int r = encode_map(enc, &pp.tmpl[0][m], bases[m], num_heads, head_dim, small_rows);
+    const int box_rows = m == 0 ? kBlockM : kv_tile_rows(head_dim);
+    int r = encode_map(enc, &pp.tmpl[0][m], bases[m], num_heads, head_dim, small_rows, box_rows);
     if (r) return r;
-    r = encode_map(enc, &pp.tmpl[1][m], bases[m], num_heads, head_dim, large_rows);
+    r = encode_map(enc, &pp.tmpl[1][m], bases[m], num_heads, head_dim, large_rows, box_rows);
     if (r) return r;
   }
   return 0;

@@ -10,9 +10,9 @@
 namespace avp {
 
 // Tiling: a work unit is (sequence, head, 256 query rows) = two 128-row Q
-// tiles that share every K/V tile; keys stream in tiles of 128.
+// tiles that share every K/V tile; keys stream in tiles of kv_tile_rows()
+// (128 for head_dim 128, 112 for head_dim 72).
 constexpr int kBlockM = 128;
-constexpr int kBlockN = 128;
 constexpr int kUnitRows = 2 * kBlockM;
 constexpr int kMapsPerSeq = 3;       // q, k, v tensor maps per sequence
 constexpr int kMapBytes = 128;       // sizeof(CUtensorMap)
@@ -65,10 +65,11 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Encode one [rows, num_heads, head_dim] bf16 map with this library's box and
-// swizzle (attn_varlen_api.cu).  Returns the CUresult.
+// Encode one [rows, num_heads, head_dim] bf16 map with this library's box
+// (box_cols(head_dim) x 1 x box_rows) and swizzle (attn_varlen_api.cu).
+// Returns the CUresult.
 int encode_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int num_heads, int head_dim,
-               uint64_t rows);
+               uint64_t rows, int box_rows);
 // Fill pp.tmpl for q, k, v at `bases` (both size classes).  Returns a CUresult.
 int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[kMapsPerSeq],
                      int num_heads, int head_dim);
@@ -88,9 +89,10 @@ struct FwdParams {
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 cudaError_t prepare_fwd(int head_dim);  // per device, before the first launch
 cudaError_t launch_fwd(int head_dim, const FwdParams& p, int grid, cudaStream_t stream);
-int fwd_threads();
+int fwd_threads(int head_dim);
 size_t fwd_smem_bytes(int head_dim);
-int box_cols(int head_dim);  // TMA box width in columns for this head_dim
+int box_cols(int head_dim);      // TMA box width in columns for this head_dim
+int kv_tile_rows(int head_dim);  // keys per K/V tile (TMA box height of the k and v maps)
 bool box_swizzle_128(int head_dim);
 
 }  // namespace avp

@@ -17,21 +17,33 @@
 //     chosen by the sequence's byte size (see kMapLargeBytes), which makes
 //     each patched map identical to the one the host encoder would produce.
 //
-//  2. fwd (persistent, one CTA per SM, 10 warps): each CTA walks the unit
-//     list with a stride of gridDim.x.  Warp roles:
+//  2. fwd (persistent, one CTA per SM): each CTA walks the unit list with a
+//     stride of gridDim.x.  Warp roles:
 //       warps 0-3  softmax for Q tile 0 (TMEM lanes 0-127 = its 128 rows)
 //       warps 4-7  softmax for Q tile 1
 //       warp  8    TMA producer: Q tiles, then a ring of K and V tiles
-//       warp  9    TMEM owner and tcgen05.mma issuer
-//     TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+DP),
-//     O1 [384,384+DP); P (bf16, packed in pairs) overwrites the first 64
-//     columns of its S and is the A operand of the P.V MMA straight from TMEM.
-//     The MMA issue order alternates the two Q tiles,
-//       S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
-//     so each softmax warpgroup has the other tile's two MMAs to hide behind.
+//       warp  9    TMEM owner and tcgen05.mma issuer (head_dim 128: both
+//                  tiles; head_dim 72: tile 0)
+//       warp 10    head_dim 72 only: tcgen05.mma issuer for tile 1
 //     Softmax is an online exp2 softmax, one row per thread, with a lazy
 //     rescale: the running max is only raised (and O rescaled in TMEM) when a
 //     row's new max exceeds it by more than kRescaleThreshold (log2 units).
+//     P (bf16, packed in pairs) is the A operand of the P.V MMA straight from
+//     TMEM.
+//
+//     head_dim 128 (TMEM: S0 [0,128), S1 [128,256), O0 [256,384),
+//     O1 [384,512)): key tiles of 128; P overwrites the first 64 columns of
+//     its S; one issuer alternates the tiles,
+//       S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
+//     so each softmax warpgroup has the other tile's two MMAs to hide behind;
+//     the tensor pipe is the bound.
+//
+//     head_dim 72 (TMEM: S0 [0,112), S1 [112,224), P0 [224,280),
+//     P1 [288,344), O0 [352,432), O1 [432,512)): key tiles of 112 so that P
+//     fits in columns of its own; S_t(j+1) is issued as soon as the softmax
+//     has read S_t(j) into registers (S_FREE), not after P_t(j).V(j); each
+//     tile has its own issuer, so neither tile's S waits in one in-order
+//     program behind the other tile's P.V.
 //
 // Head dims: 128 runs natively; 72 is padded to 80.  Both load every tile as
 // two 64-column TMA boxes with 128-byte swizzle; for 72 the second box holds
@@ -57,9 +69,8 @@ namespace avp {
 
 namespace {
 
-constexpr int kThreads = 320;
 constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;  // first MMA-issuing warp (and TMEM owner)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
 // S(j+1) of a tile overwrites the TMEM columns that P(j) of the same tile
@@ -72,6 +83,7 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr bool kStrictPvWait = ATTN_VARLEN_STRICT_PV_WAIT != 0;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 
+
 #ifndef ATTN_VARLEN_KV_STAGES
 #define ATTN_VARLEN_KV_STAGES 4
 #endif
@@ -80,9 +92,12 @@ template <int D>
 struct Cfg;
 template <>
 struct Cfg<72> {
-  static constexpr int DP = 80;   // padded head_dim (MMA K and N multiple of 16)
-  static constexpr int BW = 64;   // columns per TMA box: two boxes, the second
-                                  // holding columns 64-71 and zero fill
+  static constexpr int DP = 80;    // padded head_dim (MMA K and N multiple of 16)
+  static constexpr int BW = 64;    // columns per TMA box: two boxes, the second
+                                   // holding columns 64-71 and zero fill
+  static constexpr int KN = 112;   // keys per K/V tile
+  static constexpr bool PSEP = true;  // P in TMEM columns of its own
+  static constexpr int ISSUERS = 2;   // one MMA-issuing warp per Q tile
   static constexpr int STAGES = ATTN_VARLEN_KV_STAGES;
   static constexpr uint32_t SWZ = kSwizzle128B;
 };
@@ -90,6 +105,9 @@ template <>
 struct Cfg<128> {
   static constexpr int DP = 128;
   static constexpr int BW = 64;
+  static constexpr int KN = 128;
+  static constexpr bool PSEP = false;  // P overwrites the first half of S
+  static constexpr int ISSUERS = 1;    // one MMA-issuing warp for both Q tiles
   static constexpr int STAGES = ATTN_VARLEN_KV_STAGES;
   static constexpr uint32_t SWZ = kSwizzle128B;
 };
@@ -98,25 +116,39 @@ template <int D>
 struct Geometry {
   static constexpr int DP = Cfg<D>::DP;
   static constexpr int BW = Cfg<D>::BW;
+  static constexpr int KN = Cfg<D>::KN;
+  static constexpr bool PSEP = Cfg<D>::PSEP;
+  static constexpr int ISSUERS = Cfg<D>::ISSUERS;
+  static_assert(PSEP || ISSUERS == 1, "two issuers need P in columns of its own");
+  static constexpr int THREADS = 32 * (kMmaWarp + ISSUERS);
   static constexpr int NB = (DP + BW - 1) / BW;             // boxes per tile
   static constexpr int STAGES = Cfg<D>::STAGES;
   static constexpr uint32_t SWZ = Cfg<D>::SWZ;
-  static constexpr uint32_t BOX_BYTES = kBlockM * BW * 2;   // one box: 128 rows x BW
-  static constexpr uint32_t TILE_BYTES = NB * BOX_BYTES;    // one Q/K/V tile in smem
+  static constexpr uint32_t Q_BOX_BYTES = kBlockM * BW * 2;  // one box: 128 rows x BW
+  static constexpr uint32_t Q_TILE_BYTES = NB * Q_BOX_BYTES;
+  static constexpr uint32_t KV_BOX_BYTES = KN * BW * 2;      // one box: KN keys x BW
+  static constexpr uint32_t KV_TILE_BYTES = NB * KV_BOX_BYTES;
+  static_assert(KV_BOX_BYTES % 1024 == 0, "128B-swizzled boxes start on 1024-byte boundaries");
   static constexpr uint32_t SBO = 8 * BW * 2;               // 8-row group stride
   static constexpr uint32_t Q_OFF = 0;
-  static constexpr uint32_t KV_OFF = 2 * TILE_BYTES;
-  static constexpr uint32_t BAR_OFF = KV_OFF + STAGES * TILE_BYTES;
+  static constexpr uint32_t KV_OFF = 2 * Q_TILE_BYTES;
+  static constexpr uint32_t BAR_OFF = KV_OFF + STAGES * KV_TILE_BYTES;
   // barrier slots (8 bytes each)
   static constexpr int B_Q_FULL = 0, B_Q_EMPTY = 1, B_KV_FULL = 2, B_KV_EMPTY = 2 + STAGES,
                        B_S_FULL = 2 + 2 * STAGES, B_P_FULL = B_S_FULL + 2,
-                       B_PV_DONE = B_P_FULL + 2, B_DRAIN = B_PV_DONE + 2, NUM_BARS = B_DRAIN + 1;
+                       B_PV_DONE = B_P_FULL + 2, B_S_FREE = B_PV_DONE + 2,
+                       B_DRAIN = B_S_FREE + 2, NUM_BARS = B_DRAIN + 2;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // tmem slot, abort flag
   static constexpr uint32_t SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory above the sm_103 per-block limit");
-  static constexpr int NK_S = DP / 16;        // K-steps of S = Q K^T
-  static constexpr int NK_PV = kBlockN / 16;  // K-steps of O += P V
-  static constexpr uint32_t S_COL0 = 0, O_COL0 = 256;
+  static constexpr int NK_S = DP / 16;  // K-steps of S = Q K^T
+  static constexpr int NK_PV = KN / 16; // K-steps of O += P V
+  static_assert(KN % 16 == 0 && KN >= 64 && KN <= 128, "key tile rows");
+  // TMEM columns of S_t, P_t (bf16 pairs) and O_t
+  __host__ __device__ static constexpr uint32_t s_col(int t) { return PSEP ? (uint32_t)(t * KN) : 128u * t; }
+  __host__ __device__ static constexpr uint32_t p_col(int t) { return PSEP ? 2u * KN + 64u * t : s_col(t); }
+  __host__ __device__ static constexpr uint32_t o_col(int t) { return PSEP ? 2u * KN + 128u + DP * t : 256u + 128u * t; }
+  static_assert(o_col(1) + DP <= 512, "TMEM columns");
 };
 
 struct UnitInfo {
@@ -127,7 +159,7 @@ struct UnitInfo {
 __device__ __forceinline__ UnitInfo decode_unit(int u, const int32_t* __restrict__ order,
                                                 const int32_t* __restrict__ prefix, int num_seqs,
                                                 const int32_t* __restrict__ cu_q,
-                                                const int32_t* __restrict__ cu_k) {
+                                                const int32_t* __restrict__ cu_k, int kn) {
   // largest rank r in [0, num_seqs) with prefix[r] <= u
   int lo = 0, hi = num_seqs - 1;
   while (lo < hi) {
@@ -146,7 +178,7 @@ __device__ __forceinline__ UnitInfo decode_unit(int u, const int32_t* __restrict
   ui.head = local / pairs;
   ui.q0 = (local - ui.head * pairs) * kUnitRows;
   ui.t1 = ui.q0 + kBlockM < ui.lq;
-  ui.nkv = (ui.lk + kBlockN - 1) / kBlockN;
+  ui.nkv = (ui.lk + kn - 1) / kn;
   return ui;
 }
 
@@ -178,6 +210,25 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity))
     if (global_timer_ns() - t0 > kWaitLimitNs) return;
+}
+
+// The i-th K/V tile a unit with n key tiles puts into the ring, in the order
+// the MMA warp first uses them.  Returns true for a V tile; j = key tile.
+//   P aliasing S:  K0 V0 K1 V1 ...            (P_t(j).V(j) precedes S_t(j+1))
+//   P separate:    K0 K1 V0 K2 V1 ... K(n-1) V(n-2) V(n-1)
+//                  (S_t(j+1) is issued before P_t(j).V(j))
+template <bool kPSep>
+__device__ __forceinline__ bool kv_item_tile(int i, int n, int& j) {
+  if constexpr (!kPSep) {
+    j = i >> 1;
+    return (i & 1) != 0;
+  } else {
+    if (i == 0) { j = 0; return false; }
+    if (i == 2 * n - 1) { j = n - 1; return true; }
+    if (i & 1) { j = (i + 1) >> 1; return false; }
+    j = (i - 2) >> 1;
+    return true;
+  }
 }
 
 }  // namespace
@@ -283,7 +334,8 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
 
 // -------------------------------------------------------------------- fwd
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
+    attn_varlen_fwd_kernel(const __grid_constant__ FwdParams p) {
   using G = Geometry<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -300,17 +352,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
 
   if (threadIdx.x == 0) {
     mbar_init(bar(G::B_Q_FULL), 1);
-    mbar_init(bar(G::B_Q_EMPTY), 1);
+    mbar_init(bar(G::B_Q_EMPTY), G::ISSUERS);
     for (int s = 0; s < G::STAGES; ++s) {
       mbar_init(bar(G::B_KV_FULL + s), 1);
-      mbar_init(bar(G::B_KV_EMPTY + s), 1);
+      mbar_init(bar(G::B_KV_EMPTY + s), G::ISSUERS);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(G::B_S_FULL + t), 1);
       mbar_init(bar(G::B_P_FULL + t), kBlockM);
       mbar_init(bar(G::B_PV_DONE + t), 1);
+      mbar_init(bar(G::B_S_FREE + t), kBlockM);
     }
-    mbar_init(bar(G::B_DRAIN), 1);
+    mbar_init(bar(G::B_DRAIN + 0), 1);
+    mbar_init(bar(G::B_DRAIN + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -331,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
   if (warp == kLoadWarp) {
     // ------------------------------------------------------ TMA producer
     // The whole warp runs the loop (uniform control flow); one elected lane
-    // issues each TMA and expect-tx.
+    // issues each TMA and expect-tx.  K and V tiles enter the ring in the
+    // order the MMA warp first uses them (kv_item_tile).
     const uint32_t leader = elect_one();
     uint32_t kv_item = 0, q_use = 0;
     bool ok = true;
@@ -340,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
                         wait_bounded(b, parity, abort_flag, p.status, kStatusTimeoutLoad));
     };
     for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-      const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k);
+      const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, G::KN);
       if (ui.nkv == 0) continue;
       const uint8_t* mq = p.ws + L.maps + (size_t)ui.seq * kMapsPerSeq * kMapBytes;
       const uint8_t* mk = mq + kMapBytes;
@@ -353,31 +408,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
       __syncwarp();
       if (!(ok = wait_(bar(G::B_Q_EMPTY), (q_use & 1u) ^ 1u))) break;
       ++q_use;
-      mbar_arrive_expect_tx_if(leader, bar(G::B_Q_FULL), (ui.t1 ? 2u : 1u) * G::TILE_BYTES);
+      mbar_arrive_expect_tx_if(leader, bar(G::B_Q_FULL), (ui.t1 ? 2u : 1u) * G::Q_TILE_BYTES);
 #pragma unroll
       for (int b = 0; b < G::NB; ++b)
-        tma_load_3d_if(leader, sQ + b * G::BOX_BYTES, mq, bar(G::B_Q_FULL), b * G::BW, ui.head,
+        tma_load_3d_if(leader, sQ + b * G::Q_BOX_BYTES, mq, bar(G::B_Q_FULL), b * G::BW, ui.head,
                        ui.q0);
       if (ui.t1) {
 #pragma unroll
         for (int b = 0; b < G::NB; ++b)
-          tma_load_3d_if(leader, sQ + G::TILE_BYTES + b * G::BOX_BYTES, mq, bar(G::B_Q_FULL),
+          tma_load_3d_if(leader, sQ + G::Q_TILE_BYTES + b * G::Q_BOX_BYTES, mq, bar(G::B_Q_FULL),
                          b * G::BW, ui.head, ui.q0 + kBlockM);
       }
-      for (int j = 0; ok && j < ui.nkv; ++j) {
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t stage = kv_item % G::STAGES;
-          const uint32_t use = kv_item / G::STAGES;
-          if (!(ok = wait_(bar(G::B_KV_EMPTY + stage), (use & 1u) ^ 1u))) break;
-          mbar_arrive_expect_tx_if(leader, bar(G::B_KV_FULL + stage), G::TILE_BYTES);
-          const uint8_t* m = which ? mv : mk;
-          const uint32_t dst = sKV + stage * G::TILE_BYTES;
+      for (int i = 0; i < 2 * ui.nkv; ++i) {
+        int j;
+        const bool is_v = kv_item_tile<G::PSEP>(i, ui.nkv, j);
+        const uint32_t stage = kv_item % G::STAGES;
+        const uint32_t use = kv_item / G::STAGES;
+        if (!(ok = wait_(bar(G::B_KV_EMPTY + stage), (use & 1u) ^ 1u))) break;
+        mbar_arrive_expect_tx_if(leader, bar(G::B_KV_FULL + stage), G::KV_TILE_BYTES);
+        const uint8_t* m = is_v ? mv : mk;
+        const uint32_t dst = sKV + stage * G::KV_TILE_BYTES;
 #pragma unroll
-          for (int b = 0; b < G::NB; ++b)
-            tma_load_3d_if(leader, dst + b * G::BOX_BYTES, m, bar(G::B_KV_FULL + stage),
-                           b * G::BW, ui.head, j * kBlockN);
-          ++kv_item;
-        }
+        for (int b = 0; b < G::NB; ++b)
+          tma_load_3d_if(leader, dst + b * G::KV_BOX_BYTES, m, bar(G::B_KV_FULL + stage),
+                         b * G::BW, ui.head, j * G::KN);
+        ++kv_item;
       }
     }
     if (!ok) {
@@ -387,22 +442,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
       for (uint32_t it = first; it < kv_item; ++it)
         wait_drain(bar(G::B_KV_FULL + it % G::STAGES), (it / G::STAGES) & 1u);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp >= kMmaWarp) {
     // ------------------------------------------------------- MMA issuer
     // The whole warp runs the loop; descriptors are computed once per tile
     // base and advanced by constants, and one elected lane issues each
-    // tcgen05.mma and commit (commits track that lane's MMAs).
+    // tcgen05.mma and commit (commits track that lane's MMAs).  With two
+    // issuers, warp kMmaWarp + t issues every MMA of Q tile t, so neither
+    // tile's S waits behind the other tile's P.V in one in-order program;
+    // K/V slots and the Q buffer are released by both.
+    const int mi = warp - kMmaWarp;
     const uint32_t leader = elect_one();
-    constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, G::KN, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, G::DP, false, true);
     // K-major (Q, K) and MN-major (V) descriptors of the first tile of each
     // region; a byte offset `o` inside shared memory adds o >> 4.
     const uint64_t dq0 = smem_desc(sQ, 16, G::SBO, G::SWZ);
     const uint64_t dk0 = smem_desc(sKV, 16, G::SBO, G::SWZ);
-    const uint64_t dv0 = smem_desc(sKV, G::BOX_BYTES, G::SBO, G::SWZ);
+    const uint64_t dv0 = smem_desc(sKV, G::KV_BOX_BYTES, G::SBO, G::SWZ);
     uint32_t kv_item = 0, q_use = 0;
     uint32_t p_wait[2] = {0, 0};  // p_full phases consumed per tile
     uint32_t pv_cnt[2] = {0, 0};  // P.V groups committed per tile
+    uint32_t s_cnt[2] = {0, 0};   // S groups committed per tile
     bool ok = true;
     bool issued = false;
 
@@ -412,20 +472,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
     };
     // S_t = Q_t K^T : K from stage `ks`
     auto issue_s = [&](int t, uint32_t ks) {
-      const uint64_t qa = dq0 + ((t * G::TILE_BYTES) >> 4);
-      const uint64_t kb = dk0 + ((ks * G::TILE_BYTES) >> 4);
-      const uint32_t d = tmem + G::S_COL0 + 128u * t;
+      const uint64_t qa = dq0 + ((t * G::Q_TILE_BYTES) >> 4);
+      const uint64_t kb = dk0 + ((ks * G::KV_TILE_BYTES) >> 4);
+      const uint32_t d = tmem + G::s_col(t);
 #pragma unroll
       for (int k = 0; k < G::NK_S; ++k) {
-        const uint32_t off = ((k * 16 / G::BW) * G::BOX_BYTES + ((k * 16) % G::BW) * 2) >> 4;
-        mma_ss_if(leader, d, qa + off, kb + off, idesc_s, k > 0 ? 1u : 0u);
+        const uint32_t box = (uint32_t)(k * 16 / G::BW);
+        const uint32_t col_b = (uint32_t)((k * 16) % G::BW) * 2;
+        mma_ss_if(leader, d, qa + ((box * G::Q_BOX_BYTES + col_b) >> 4),
+                  kb + ((box * G::KV_BOX_BYTES + col_b) >> 4), idesc_s, k > 0 ? 1u : 0u);
       }
     };
-    // O_t (+)= P_t V : V from stage `vs`, P from TMEM (aliasing S_t)
+    // O_t (+)= P_t V : V from stage `vs`, P from TMEM
     auto issue_pv = [&](int t, uint32_t vs, bool acc) {
-      const uint64_t vb = dv0 + ((vs * G::TILE_BYTES) >> 4);
-      const uint32_t d = tmem + G::O_COL0 + 128u * t;
-      const uint32_t a = tmem + G::S_COL0 + 128u * t;
+      const uint64_t vb = dv0 + ((vs * G::KV_TILE_BYTES) >> 4);
+      const uint32_t d = tmem + G::o_col(t);
+      const uint32_t a = tmem + G::p_col(t);
 #pragma unroll
       for (int k = 0; k < G::NK_PV; ++k)
         mma_ts_if(leader, d, a + 8u * k, vb + ((k * 16 * G::BW * 2) >> 4), idesc_pv,
@@ -437,88 +499,141 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
       if (!kStrictPvWait || pv_cnt[t] == 0) return true;
       return wait_(bar(G::B_PV_DONE + t), (pv_cnt[t] - 1) & 1u);
     };
+    auto stage_of = [](uint32_t it) { return it % G::STAGES; };
+    auto kv_full = [&](uint32_t it) -> bool {
+      return wait_(bar(G::B_KV_FULL + it % G::STAGES), (it / G::STAGES) & 1u);
+    };
 
     for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-      const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k);
+      const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, G::KN);
       if (ui.nkv == 0) continue;
       if (!(ok = wait_(bar(G::B_Q_FULL), q_use & 1u))) break;
       ++q_use;
-      // j = 0: S0, S1 from K_0
-      {
-        const uint32_t it = kv_item;
-        if (!(ok = wait_(bar(G::B_KV_FULL + it % G::STAGES), (it / G::STAGES) & 1u))) break;
-        ok = wait_pv_idle(0);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s(0, it % G::STAGES);
-        mma_commit_if(leader, bar(G::B_S_FULL + 0));
-        if (ui.t1) {
-          ok = wait_pv_idle(1);
+      issued = true;
+      const int nt = ui.t1 ? 2 : 1;
+      if constexpr (G::PSEP) {
+        // Tile t = mi.  Order per key tile j:  S_t(j) | P_t(j-1).V(j-1).
+        // S_t(j) only needs the softmax to have read S_t(j-1) (S_FREE), so
+        // it runs while that softmax is still in its exp2 phase.  A unit
+        // without a second Q tile still has issuer 1 take part in the slot
+        // releases, after each slot has filled, so no barrier runs ahead.
+        const int t = mi;
+        const bool has = t == 0 || ui.t1;
+        auto release = [&](uint32_t b) {
+          if (has)
+            mma_commit_if(leader, b);
+          else if (leader)
+            mbar_arrive(b);
+        };
+        const int n = ui.nkv;
+        for (int j = 0; ok && j <= n; ++j) {
+          if (j < n) {
+            const uint32_t itk = kv_item + (j == 0 ? 0u : 2u * j - 1u);
+            if (!(ok = kv_full(itk))) break;
+            if (has) {
+              if (s_cnt[t] > 0 && !(ok = wait_(bar(G::B_S_FREE + t), (s_cnt[t] - 1) & 1u))) break;
+              tc_fence_after();
+              issue_s(t, stage_of(itk));
+              mma_commit_if(leader, bar(G::B_S_FULL + t));
+              ++s_cnt[t];
+            }
+            release(bar(G::B_KV_EMPTY + stage_of(itk)));
+            if (j == n - 1) release(bar(G::B_Q_EMPTY));
+          }
+          if (j >= 1) {
+            const uint32_t itv = kv_item + (j == n ? 2u * n - 1u : 2u * j);
+            if (!(ok = kv_full(itv))) break;
+            if (has) {
+              if (!(ok = wait_(bar(G::B_P_FULL + t), p_wait[t] & 1u))) break;
+              ++p_wait[t];
+              tc_fence_after();
+              issue_pv(t, stage_of(itv), j > 1);
+              mma_commit_if(leader, bar(G::B_PV_DONE + t));
+            }
+            release(bar(G::B_KV_EMPTY + stage_of(itv)));
+          }
+        }
+        (void)nt;
+      } else {
+        // Order:  S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
+        // S_t(j+1) overwrites P_t(j) and is queued right behind P_t(j).V(j).
+        {
+          const uint32_t it = kv_item;
+          if (!(ok = kv_full(it))) break;
+          ok = wait_pv_idle(0);
           if (!ok) break;
           tc_fence_after();
-          issue_s(1, it % G::STAGES);
-          mma_commit_if(leader, bar(G::B_S_FULL + 1));
-        }
-        mma_commit_if(leader, bar(G::B_KV_EMPTY + it % G::STAGES));
-        if (ui.nkv == 1) mma_commit_if(leader, bar(G::B_Q_EMPTY));
-        issued = true;
-      }
-      for (int j = 0; ok && j < ui.nkv; ++j) {
-        const uint32_t itv = kv_item + 2 * j + 1;
-        const uint32_t itk = itv + 1;
-        const bool more = j + 1 < ui.nkv;
-        if (!(ok = wait_(bar(G::B_KV_FULL + itv % G::STAGES), (itv / G::STAGES) & 1u))) break;
-        // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
-        if (!(ok = wait_(bar(G::B_P_FULL + 0), p_wait[0] & 1u))) break;
-        ++p_wait[0];
-        tc_fence_after();
-        issue_pv(0, itv % G::STAGES, j > 0);
-        mma_commit_if(leader, bar(G::B_PV_DONE + 0));
-        ++pv_cnt[0];
-        if (more) {
-          if (!(ok = wait_(bar(G::B_KV_FULL + itk % G::STAGES), (itk / G::STAGES) & 1u))) break;
-          ok = wait_pv_idle(0);
-        if (!ok) break;
-          tc_fence_after();
-          issue_s(0, itk % G::STAGES);
+          issue_s(0, stage_of(it));
           mma_commit_if(leader, bar(G::B_S_FULL + 0));
-        }
-        // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
-        if (ui.t1) {
-          if (!(ok = wait_(bar(G::B_P_FULL + 1), p_wait[1] & 1u))) break;
-          ++p_wait[1];
-          tc_fence_after();
-          issue_pv(1, itv % G::STAGES, j > 0);
-          mma_commit_if(leader, bar(G::B_PV_DONE + 1));
-          ++pv_cnt[1];
-        }
-        mma_commit_if(leader, bar(G::B_KV_EMPTY + itv % G::STAGES));
-        if (more) {
           if (ui.t1) {
             ok = wait_pv_idle(1);
           if (!ok) break;
             tc_fence_after();
-            issue_s(1, itk % G::STAGES);
+            issue_s(1, stage_of(it));
             mma_commit_if(leader, bar(G::B_S_FULL + 1));
           }
-          mma_commit_if(leader, bar(G::B_KV_EMPTY + itk % G::STAGES));
-          if (j + 2 == ui.nkv) mma_commit_if(leader, bar(G::B_Q_EMPTY));
+          mma_commit_if(leader, bar(G::B_KV_EMPTY + stage_of(it)));
+          if (ui.nkv == 1) mma_commit_if(leader, bar(G::B_Q_EMPTY));
+        }
+        for (int j = 0; ok && j < ui.nkv; ++j) {
+          const uint32_t itv = kv_item + 2 * j + 1;
+          const uint32_t itk = itv + 1;
+          const bool more = j + 1 < ui.nkv;
+          if (!(ok = kv_full(itv))) break;
+          // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
+          if (!(ok = wait_(bar(G::B_P_FULL + 0), p_wait[0] & 1u))) break;
+          ++p_wait[0];
+          tc_fence_after();
+          issue_pv(0, stage_of(itv), j > 0);
+          mma_commit_if(leader, bar(G::B_PV_DONE + 0));
+          ++pv_cnt[0];
+          if (more) {
+            if (!(ok = kv_full(itk))) break;
+            ok = wait_pv_idle(0);
+          if (!ok) break;
+            tc_fence_after();
+            issue_s(0, stage_of(itk));
+            mma_commit_if(leader, bar(G::B_S_FULL + 0));
+          }
+          // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
+          if (ui.t1) {
+            if (!(ok = wait_(bar(G::B_P_FULL + 1), p_wait[1] & 1u))) break;
+            ++p_wait[1];
+            tc_fence_after();
+            issue_pv(1, stage_of(itv), j > 0);
+            mma_commit_if(leader, bar(G::B_PV_DONE + 1));
+            ++pv_cnt[1];
+          }
+          mma_commit_if(leader, bar(G::B_KV_EMPTY + stage_of(itv)));
+          if (more) {
+            if (ui.t1) {
+              ok = wait_pv_idle(1);
+          if (!ok) break;
+              tc_fence_after();
+              issue_s(1, stage_of(itk));
+              mma_commit_if(leader, bar(G::B_S_FULL + 1));
+            }
+            mma_commit_if(leader, bar(G::B_KV_EMPTY + stage_of(itk)));
+            if (j + 2 == ui.nkv) mma_commit_if(leader, bar(G::B_Q_EMPTY));
+          }
         }
       }
       kv_item += 2u * (uint32_t)ui.nkv;
     }
     if (issued) {
       // every MMA this warp issued must be finished before TMEM is freed
-      mma_commit_if(leader, bar(G::B_DRAIN));
-      wait_drain(bar(G::B_DRAIN), 0);
+      mma_commit_if(leader, bar(G::B_DRAIN + mi));
+      wait_drain(bar(G::B_DRAIN + mi), 0);
     }
   } else {
     // --------------------------------------------------------- softmax
+    constexpr int KN = G::KN;
     const int t = warp >> 2;                       // Q tile of this warpgroup
     const int r = threadIdx.x & 127;               // row in the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_off + G::S_COL0 + 128u * t;
-    const uint32_t tO = tmem + lane_off + G::O_COL0 + 128u * t;
+    const uint32_t tS = tmem + lane_off + G::s_col(t);
+    const uint32_t tP = tmem + lane_off + G::p_col(t);
+    const uint32_t tO = tmem + lane_off + G::o_col(t);
     const float sl2 = p.scale_log2;
     uint32_t s_wait = 0, p_cnt = 0;
     bool ok = true;
@@ -529,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
     };
 
     for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-      const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k);
+      const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, KN);
       if (t == 1 && !ui.t1) continue;
       const int row = ui.q0 + kBlockM * t + r;
       const bool valid = row < ui.lq;
@@ -547,19 +662,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
         if (!(ok = wait_(bar(G::B_S_FULL + t), s_wait & 1u))) break;
         ++s_wait;
         tc_fence_after();
-        uint32_t s[128];
+        uint32_t s[KN];
         // keys past the end of the sequence in its last tile
-        const int lim = ui.lk - j * kBlockN;
-        const bool tail = (j == ui.nkv - 1) && lim < kBlockN;
+        const int lim = ui.lk - j * KN;
+        const bool tail = lim < KN;  // only the last key tile can be partial
         tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
         tmem_wait_ld();
         reg_fence(s, 0, 64);
         tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+        if constexpr (KN == 128)
+          tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+        else
+          tmem_ld16(tS + 96, *reinterpret_cast<uint32_t(*)[16]>(&s[96]));
         float mx0, mx1, mx2, mx3;
         if (!tail) {
-          // row max of the first half while the second half is in flight
+          // row max of the first 64 keys while the rest is in flight
           mx0 = __uint_as_float(s[0]);
           mx1 = __uint_as_float(s[1]);
           mx2 = __uint_as_float(s[2]);
@@ -572,12 +690,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
             mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
           }
           tmem_wait_ld();
-          reg_fence(s, 64, 64);
+          reg_fence(s, 64, KN - 64);
         } else {
           tmem_wait_ld();
-          reg_fence(s, 64, 64);
+          reg_fence(s, 64, KN - 64);
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
+          for (int c = 0; c < KN; ++c)
             if (c >= lim) s[c] = __float_as_uint(-INFINITY);
           mx0 = mx1 = mx2 = mx3 = -INFINITY;
 #pragma unroll
@@ -588,8 +706,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
             mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
           }
         }
+        if constexpr (G::PSEP) {
+          // S_t is in registers: the MMA warp may compute the next S_t now
+          tc_fence_before();
+          mbar_arrive(bar(G::B_S_FREE + t));
+        }
 #pragma unroll
-        for (int c = 64; c < 128; c += 8) {
+        for (int c = 64; c < KN; c += 8) {
           mx0 = fmax3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
           mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
           mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
@@ -624,11 +747,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
         const float2 c2 = make_float2(sl2, sl2);
         const float2 nm2 = make_float2(-m, -m);
         float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-        uint32_t pk[64];
+        uint32_t pk[KN / 2];
+        auto exp_pairs = [&](int c0, int c1) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int c = 32 * h; c < 32 * h + 32; c += 2) {
+          for (int c = c0; c < c1; c += 2) {
             float2 a = __ffma2_rn(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])),
                                   c2, nm2);
             float2 b = __ffma2_rn(make_float2(__uint_as_float(s[2 * c + 2]),
@@ -642,7 +764,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_varlen_fwd_kernel(const __gr
             pk[c] = pack_bf16x2(a.x, a.y);
             pk[c + 1] = pack_bf16x2(b.x, b.y);
           }
-          tmem_st32(tS + 32 * h, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * h]));
+        };
+        if constexpr (G::PSEP) {
+          exp_pairs(0, KN / 2);
+          // P_t(j-1) must have been read by its P.V before it is overwritten
+          if (p_cnt > 0 && !(ok = wait_(bar(G::B_PV_DONE + t), (p_cnt - 1) & 1u))) break;
+          tc_fence_after();
+          static_assert(KN == 112, "P store split below assumes 56 packed columns");
+          tmem_st32(tP + 0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+          tmem_st16(tP + 32, *reinterpret_cast<const uint32_t(*)[16]>(&pk[32]));
+          tmem_st8(tP + 48, *reinterpret_cast<const uint32_t(*)[8]>(&pk[48]));
+        } else {
+          // P_t overwrites the first half of S_t, already in registers
+#pragma unroll
+          for (int h = 0; h < KN / 64; ++h) {
+            exp_pairs(32 * h, 32 * h + 32);
+            tmem_st32(tP + 32 * h, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * h]));
+          }
         }
         tmem_wait_st();
         l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
@@ -691,7 +829,7 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
 
 template <int D>
 static cudaError_t launch_fwd_t(const FwdParams& p, int grid, cudaStream_t stream) {
-  attn_varlen_fwd_kernel<D><<<grid, kThreads, Geometry<D>::SMEM_BYTES, stream>>>(p);
+  attn_varlen_fwd_kernel<D><<<grid, Geometry<D>::THREADS, Geometry<D>::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -713,13 +851,17 @@ cudaError_t launch_fwd(int head_dim, const FwdParams& p, int grid, cudaStream_t 
   return cudaErrorInvalidValue;
 }
 
-int fwd_threads() { return kThreads; }
+int fwd_threads(int head_dim) {
+  return head_dim == 72 ? Geometry<72>::THREADS : Geometry<128>::THREADS;
+}
 
 size_t fwd_smem_bytes(int head_dim) {
   return head_dim == 72 ? Geometry<72>::SMEM_BYTES : Geometry<128>::SMEM_BYTES;
 }
 
 int box_cols(int head_dim) { return head_dim == 72 ? Cfg<72>::BW : Cfg<128>::BW; }
+
+int kv_tile_rows(int head_dim) { return head_dim == 72 ? Cfg<72>::KN : Cfg<128>::KN; }
 
 bool box_swizzle_128(int head_dim) {
   return (head_dim == 72 ? Cfg<72>::SWZ : Cfg<128>::SWZ) == kSwizzle128B;
