@@ -38,19 +38,27 @@ def device_inputs(x: dict, device):
             torch.from_numpy(x["cu_q"]).to(device), torch.from_numpy(x["cu_k"]).to(device))
 
 
-def run_cuda(vlp, x: dict, device="cuda", out_fill: int | None = None):
+def run_cuda(vlp, x: dict, device="cuda", out_fill: int | None = None,
+             caller_workspace: bool = False):
     """Run the CUDA path; returns the output as bf16 bits (uint16, [T, H, D]).
 
     ``out_fill``: int16 bit pattern to pre-fill the output with (default:
-    torch.empty_like)."""
+    torch.empty_like).  ``caller_workspace``: pass a caller-owned workspace of
+    workspace_size(num_seqs) bytes (that entry point never splits units)."""
     import torch
     t, cu_q, cu_k = device_inputs(x, device)
     out = None
     if out_fill is not None:
         out = torch.full(t["q"].shape, out_fill, dtype=torch.int16,
                          device=device).view(torch.bfloat16)
-    out = vlp.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, out=out)
-    vlp.check()
+    if caller_workspace:
+        ws = torch.zeros(vlp.workspace_size(len(x["cu_q"]) - 1), dtype=torch.uint8,
+                         device=device)
+        out = vlp.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, out=out, workspace=ws)
+        vlp.check(workspace=ws)
+    else:
+        out = vlp.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, out=out)
+        vlp.check()
     return to_bits(out)
 
 
@@ -114,3 +122,14 @@ def check_sampled(vlp, w, rows_per_head: int, device="cuda"):
     rows = sample_rows(w, rows_per_head)
     ref = oracle.attn_rows(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], rows)
     return assert_close(got[rows[:, 0], rows[:, 1]], ref, w.name)
+
+
+def check_rows(vlp, w, rows: np.ndarray, device="cuda", caller_workspace=False, x=None):
+    """Given (token, head) output rows of workload `w` against the oracle;
+    returns the CUDA output (bf16 bits) for further comparisons."""
+    x = make_inputs(w) if x is None else x
+    got = run_cuda(vlp, x, device, caller_workspace=caller_workspace)
+    ref = oracle.attn_rows(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], rows)
+    assert_close(got[rows[:, 0], rows[:, 1]], ref,
+                 w.name + (" caller workspace" if caller_workspace else ""))
+    return got

@@ -5,8 +5,8 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_helpers import (assert_close, check_full, check_sampled, device_inputs, run_cuda,
-                         to_bits)
+from gpu_helpers import (abs_bits, assert_close, bf16_bound, check_full, check_rows,
+                         check_sampled, device_inputs, run_cuda, to_bits)
 from workloads import C1, C2, C3, C4, C5, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -88,9 +88,12 @@ def test_num_seqs_zero_is_a_noop(cuda_lib):
 
 def test_packing_invariance_bitwise(cuda_lib):
     """The packed batch equals each member run alone, bit for bit (tiles
-    start at sequence starts, so every row sees the same arithmetic)."""
+    start at sequence starts, so every row sees the same arithmetic).  Run
+    with caller-owned workspaces, which never split a unit's key range: the
+    library-owned workspace may split the units of the grid's last partial
+    wave, and which units those are depends on the whole batch."""
     x = make_inputs(C5)
-    packed = run_cuda(cuda_lib, x)
+    packed = run_cuda(cuda_lib, x, caller_workspace=True)
     cu = x["cu_q"]
     for i in range(len(cu) - 1):
         if cu[i + 1] <= cu[i]:
@@ -99,7 +102,8 @@ def test_packing_invariance_bitwise(cuda_lib):
         alone = {"q": x["q"][sl], "k": x["k"][sl], "v": x["v"][sl],
                  "cu_q": np.array([0, cu[i + 1] - cu[i]], np.int32),
                  "cu_k": np.array([0, cu[i + 1] - cu[i]], np.int32)}
-        np.testing.assert_array_equal(run_cuda(cuda_lib, alone), packed[sl])
+        np.testing.assert_array_equal(run_cuda(cuda_lib, alone, caller_workspace=True),
+                                      packed[sl])
 
 
 def test_deterministic(cuda_lib):
@@ -162,9 +166,12 @@ def test_running_max_huge_jump(cuda_lib, D):
 
 
 def test_caller_workspace_on_two_streams(cuda_lib):
+    """Two calls with their own workspaces on two streams agree bit for bit
+    with a single caller-workspace call (the default entry point may split C1's
+    units along keys, so it is compared with the oracle elsewhere)."""
     import torch
     x = make_inputs(C1)
-    want = run_cuda(cuda_lib, x)
+    want = run_cuda(cuda_lib, x, caller_workspace=True)
     t, cu_q, cu_k = device_inputs(x, "cuda")
     outs = []
     for _ in range(2):
@@ -186,3 +193,51 @@ def test_errors_raise(cuda_lib):
     with pytest.raises(AttnVarlenError) as e:
         cuda_lib.attn_varlen_fwd(q, q, q, cu, cu)
     assert e.value.code == -2
+
+
+def _tail_rows(w, extra_per_head=48, seed=11):
+    """The last 8 query rows of every head plus a seeded sample."""
+    cu_q, _ = w.cu_seqlens()
+    end = int(cu_q[-1])
+    rng = np.random.default_rng(seed)
+    rows = []
+    for h in range(w.num_heads):
+        last = np.arange(max(int(cu_q[0]), end - 8), end)
+        pick = rng.choice(np.arange(int(cu_q[0]), end), size=extra_per_head, replace=False)
+        toks = np.unique(np.concatenate([last, pick]))
+        rows.append(np.stack([toks, np.full(toks.size, h)], axis=1))
+    return np.concatenate(rows).astype(np.int64)
+
+
+@pytest.mark.parametrize("D", [72, 128])
+def test_tail_split_one_unit_over_the_grid(cuda_lib, D):
+    """152 full units plus one more: on a 152-SM GB300 the last unit (7
+    query rows against all 38919 keys) is cut into many key chunks whose
+    partials are merged; the caller-workspace path computes it whole."""
+    w = Workload(f"tail_153_units_D{D}", (152 * 256 + 7,), 1, D, seed=31 + D)
+    rows = _tail_rows(w)
+    x = make_inputs(w)
+    # both meet the bar against the oracle; they may differ in the last bits
+    # where the fp32 sums were taken in another order
+    check_rows(cuda_lib, w, rows, x=x)
+    check_rows(cuda_lib, w, rows, x=x, caller_workspace=True)
+
+
+def test_tail_split_mixed_batch(cuda_lib):
+    """Fewer units than SMs, so every unit is in the last partial wave: units
+    of 36, 27, 19, 18, 1 and 0 key tiles are cut into different numbers of
+    chunks.  Every row against the oracle, through both entry points."""
+    lens_q = (3000, 1, 700, 0, 2048, 5, 300)
+    lens_k = (2000, 4000, 0, 9, 2048, 3000, 1)
+    w = Workload("tail_mixed", lens_q, 2, 72, seed=77, seq_lens_k=lens_k)
+    x = make_inputs(w)
+    check_full(cuda_lib, w, x=x, short_sequences=True)
+    got = run_cuda(cuda_lib, x, caller_workspace=True)
+    ref = oracle.attn_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"])
+    live = np.zeros(got.shape[0], bool)
+    cu = x["cu_q"]
+    for i in range(len(cu) - 1):
+        live[cu[i]:cu[i + 1]] = True
+    absv = oracle.attn_varlen(x["q"], x["k"], abs_bits(x["v"]), x["cu_q"], x["cu_k"])
+    assert_close(got[live], ref[live], "tail_mixed caller workspace",
+                 bound=bf16_bound(ref[live], absv[live]))

@@ -137,8 +137,10 @@ int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[
 
 namespace {
 
+// `split_cap` > 0: the workspace holds a tail-split region for that many
+// items right after ws_layout(num_seqs).total.
 int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const int32_t* cu_k,
-        int num_seqs, int num_heads, int head_dim, void* out, void* ws, int dev,
+        int num_seqs, int num_heads, int head_dim, void* out, void* ws, int split_cap, int dev,
         DeviceState& st, cudaStream_t stream) {
   avp::PlanParams pp;
   std::memset(&pp, 0, sizeof(pp));
@@ -150,12 +152,19 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const 
   pp.cu_q = cu_q;
   pp.cu_k = cu_k;
   pp.ws = static_cast<uint8_t*>(ws);
+  uint8_t* split = split_cap > 0 ? pp.ws + avp::ws_layout(num_seqs).total : nullptr;
+  pp.split = split;
+  pp.split_cap = split_cap;
+  pp.grid = st.sm_count;
+  pp.kv_rows = avp::kv_tile_rows(head_dim);
   pp.num_seqs = num_seqs;
   pp.num_heads = num_heads;
   pp.row_bytes = num_heads * head_dim * 2;
 
   avp::FwdParams fp;
   fp.ws = static_cast<const uint8_t*>(ws);
+  fp.split = split;
+  fp.split_cap = split_cap;
   fp.status = static_cast<int*>(ws);
   fp.cu_q = cu_q;
   fp.cu_k = cu_k;
@@ -249,9 +258,13 @@ int attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* 
   DeviceState& st = g_dev[dev];
   if ((rc = probe_device(dev, st))) return rc;
   if ((rc = get_encoder())) return rc;
-  if ((rc = ensure_workspace(st, avp::ws_layout(num_seqs).total))) return rc;
-  return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, st.ws, dev,
-             st, stream);
+  // the library-owned workspace also holds the tail-split region (one item
+  // per CTA of the persistent grid)
+  const int cap = st.sm_count;
+  if ((rc = ensure_workspace(st, avp::ws_layout(num_seqs).total + avp::split_layout(cap).total)))
+    return rc;
+  return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, st.ws, cap,
+             dev, st, stream);
 }
 
 int attn_varlen_fwd_ws(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
@@ -269,7 +282,7 @@ int attn_varlen_fwd_ws(const void* q, const void* k, const void* v, const int32_
   if ((rc = probe_device(dev, st))) return rc;
   if ((rc = get_encoder())) return rc;
   return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, workspace,
-             dev, st, stream);
+             0, dev, st, stream);
 }
 
 int attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v,
@@ -298,7 +311,7 @@ int attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v,
   // kernel rewrites everything else the attention kernel reads
   cudaError_t me = cudaMemsetAsync(ws, 0, sizeof(int), stream);
   if (me != cudaSuccess) return fail_cuda(me);
-  return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, ws, dev,
+  return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, ws, 0, dev,
              st, stream);
 }
 

@@ -71,6 +71,7 @@ namespace {
 
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;  // first MMA-issuing warp (and TMEM owner)
+constexpr int kItemDepth = 4; // work items handed from the producer to the other roles
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
 // S(j+1) of a tile overwrites the TMEM columns that P(j) of the same tile
@@ -82,6 +83,12 @@ constexpr float kRescaleThreshold = 8.0f;
 #endif
 constexpr bool kStrictPvWait = ATTN_VARLEN_STRICT_PV_WAIT != 0;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
+#ifndef ATTN_VARLEN_TAIL_SPLIT
+#define ATTN_VARLEN_TAIL_SPLIT 1
+#endif
+// A split pays off only if it shortens the tail by more than the partial
+// write and merge cost, counted in key tiles of work.
+constexpr int kMergeTiles = 8;
 
 
 #ifndef ATTN_VARLEN_KV_STAGES
@@ -137,13 +144,18 @@ struct Geometry {
   static constexpr int B_Q_FULL = 0, B_Q_EMPTY = 1, B_KV_FULL = 2, B_KV_EMPTY = 2 + STAGES,
                        B_S_FULL = 2 + 2 * STAGES, B_P_FULL = B_S_FULL + 2,
                        B_PV_DONE = B_P_FULL + 2, B_S_FREE = B_PV_DONE + 2,
-                       B_DRAIN = B_S_FREE + 2, NUM_BARS = B_DRAIN + 2;
-  static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // tmem slot, abort flag
-  static constexpr uint32_t SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
+                       B_DRAIN = B_S_FREE + 2, B_ITEM_FULL = B_DRAIN + 2,
+                       B_ITEM_EMPTY = B_ITEM_FULL + kItemDepth,
+                       NUM_BARS = B_ITEM_EMPTY + kItemDepth;
+  // tmem slot, abort flag, then the item ring (kItemDepth int32)
+  static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr uint32_t SMEM_BYTES = MISC_OFF + 8 + 4 * kItemDepth + 1024;  // + alignment slack
+  static constexpr int ITEM_CONSUMERS = 8 + ISSUERS;  // warps that read each ring entry
   static_assert(SMEM_BYTES <= 232448, "shared memory above the sm_103 per-block limit");
   static constexpr int NK_S = DP / 16;  // K-steps of S = Q K^T
   static constexpr int NK_PV = KN / 16; // K-steps of O += P V
   static_assert(KN % 16 == 0 && KN >= 64 && KN <= 128, "key tile rows");
+  static_assert(DP + 2 <= kPartRowMax, "partial row");
   // TMEM columns of S_t, P_t (bf16 pairs) and O_t
   __host__ __device__ static constexpr uint32_t s_col(int t) { return PSEP ? (uint32_t)(t * KN) : 128u * t; }
   __host__ __device__ static constexpr uint32_t p_col(int t) { return PSEP ? 2u * KN + 64u * t : s_col(t); }
@@ -152,7 +164,10 @@ struct Geometry {
 };
 
 struct UnitInfo {
-  int seq, head, q0, lq, lk, qbase, nkv;
+  int seq, head, q0, lq, lk, qbase;
+  int jb, nkv;     // this item's key tiles: [jb, jb + nkv)
+  int chunks;      // items the unit is split into (1: not split)
+  int part, part0, tail;  // split items: partial slot, the unit's first slot, tail unit
   bool t1;  // second Q tile holds at least one row
 };
 
@@ -179,6 +194,41 @@ __device__ __forceinline__ UnitInfo decode_unit(int u, const int32_t* __restrict
   ui.q0 = (local - ui.head * pairs) * kUnitRows;
   ui.t1 = ui.q0 + kBlockM < ui.lq;
   ui.nkv = (ui.lk + kn - 1) / kn;
+  ui.jb = 0;
+  ui.chunks = 1;
+  ui.part = ui.part0 = ui.tail = -1;
+  return ui;
+}
+
+// Work item -> unit and key-tile range.  Items below split_start are whole
+// units; the others are chunks of the tail units (tail_prefix).
+__device__ __forceinline__ UnitInfo decode_item(int it, const int32_t* __restrict__ order,
+                                                const int32_t* __restrict__ prefix, int num_seqs,
+                                                const int32_t* __restrict__ cu_q,
+                                                const int32_t* __restrict__ cu_k, int kn,
+                                                int split_start, int num_units,
+                                                const int32_t* __restrict__ tail_prefix) {
+  if (it < split_start) return decode_unit(it, order, prefix, num_seqs, cu_q, cu_k, kn);
+  const int k = it - split_start;
+  int lo = 0, hi = num_units - split_start - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(tail_prefix + mid) <= k) lo = mid; else hi = mid - 1;
+  }
+  UnitInfo ui = decode_unit(split_start + lo, order, prefix, num_seqs, cu_q, cu_k, kn);
+  const int c0 = __ldg(tail_prefix + lo);
+  const int chunks = __ldg(tail_prefix + lo + 1) - c0;
+  if (chunks > 1) {
+    const int c = k - c0;
+    const int jb = (int)(((long long)c * ui.nkv) / chunks);
+    const int je = (int)(((long long)(c + 1) * ui.nkv) / chunks);
+    ui.jb = jb;
+    ui.nkv = je - jb;
+    ui.chunks = chunks;
+    ui.part = k;
+    ui.part0 = c0;
+    ui.tail = lo;
+  }
   return ui;
 }
 
@@ -326,10 +376,172 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
     const int lq = p.cu_q[i + 1] - p.cu_q[i];
     run += lq > 0 ? p.num_heads * ((lq + kUnitRows - 1) / kUnitRows) : 0;
   }
-  if (tid == 0) {
-    prefix[N] = s_carry;
-    hdr[1] = s_carry;
+  if (tid == 0) prefix[N] = s_carry;
+  __syncthreads();
+
+  // 4. tail split: the units of the last, partial wave of the persistent
+  //    grid are cut along the key range so that the tail fills the grid.
+  //    Chunk count of tail unit i: ceil(nkv_i / T) with the smallest key-tile
+  //    budget T whose total fits the grid.  Everything runs on chip: the
+  //    tail units' key-tile counts go to shared memory (s_key is free now),
+  //    one warp searches T with shuffle reductions.
+  const int U = s_carry;
+  const int R = p.grid > 0 ? U % p.grid : 0;
+  const bool try_split = ATTN_VARLEN_TAIL_SPLIT && p.split_cap >= p.grid && p.grid > 0 &&
+                         R > 0 && R <= kLptMaxSeqs;
+  const int t0 = U - R;  // first tail unit
+  if (try_split) {
+    for (int r = tid; r < N; r += nt) {
+      const int ua = max(prefix[r], t0), ub = prefix[r + 1];
+      if (ua < ub) {
+        const int sq = order[r];
+        const int lk = p.cu_k[sq + 1] - p.cu_k[sq];
+        const int nkv = lk > 0 ? (lk + p.kv_rows - 1) / p.kv_rows : 0;
+        for (int u = ua; u < ub; ++u) s_key[u - t0] = nkv;
+      }
+    }
   }
+  __syncthreads();
+  if (warp == 0) {
+    int split_start = U, items = U;
+    if (try_split) {
+      int maxn = 0;
+      for (int i = lane; i < R; i += 32) maxn = max(maxn, s_key[i]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) maxn = max(maxn, __shfl_xor_sync(0xffffffffu, maxn, o));
+      int lo = 1, hi = maxn > 1 ? maxn : 1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        int sum = 0;
+        for (int i = lane; i < R; i += 32) sum += s_key[i] > mid ? (s_key[i] + mid - 1) / mid : 1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (sum <= p.grid) hi = mid; else lo = mid + 1;
+      }
+      if (lo + kMergeTiles < maxn) {
+        // chunk counts -> exclusive prefix (each lane a contiguous block)
+        const SplitLayout SL = split_layout(p.split_cap);
+        int* tp = reinterpret_cast<int*>(p.split + SL.prefix);
+        const int per = (R + 31) / 32, i0 = lane * per, i1 = min(R, i0 + per);
+        int mine = 0;
+        for (int i = i0; i < i1; ++i) mine += s_key[i] > lo ? (s_key[i] + lo - 1) / lo : 1;
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int run_items = incl - mine;
+        for (int i = i0; i < i1; ++i) {
+          tp[i] = run_items;
+          run_items += s_key[i] > lo ? (s_key[i] + lo - 1) / lo : 1;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (lane == 0) tp[R] = total;
+        split_start = t0;
+        items = t0 + total;
+      }
+    }
+    if (lane == 0) {
+      hdr[1] = U;
+      hdr[2] = items;
+      hdr[3] = split_start;
+      hdr[kHdrNextItem] = 0;
+      s_warp[0] = U - split_start;  // tail units whose row counters must be zero
+    }
+  }
+  __syncthreads();
+  const int nzero = s_warp[0];
+  if (nzero > 0) {
+    int* cnt = reinterpret_cast<int*>(p.split + split_layout(p.split_cap).counters);
+    for (int i = tid; i < nzero * 2 * kBlockM; i += nt) cnt[i] = 0;
+  }
+}
+
+// Epilogue of one chunk of a split unit for one row (softmax warpgroup t,
+// row r): the unnormalised O row and its (m, l) go to partial slot `part`;
+// the last chunk of the unit to finish that row (a counter per row and Q
+// tile) merges the unit's chunks in chunk order,
+//   m* = max_c m_c,  O = sum_c 2^(m_c - m*) O_c,  l = sum_c 2^(m_c - m*) l_c,
+// and writes O / l as bf16.  Each thread works alone (no barrier).  A slot
+// is column-major ([column][128 rows]) so that a warp's stores and loads of
+// one column are one 128-byte line; partials bypass L1, and the counter's
+// acquire-release add orders them between the chunks.
+template <int D>
+__device__ __noinline__ void split_epilogue(uint8_t* parts_base, int* counters, uint32_t tO, int t,
+                                            int r, float m, float l, uint16_t* orow, bool valid,
+                                            int part, int part0, int tail, int chunks) {
+  using G = Geometry<D>;
+  constexpr size_t kSlot = (size_t)kPartRowMax * kBlockM;  // floats per (chunk, tile) slot
+  float* parts = reinterpret_cast<float*>(parts_base);
+  float* mine = parts + (size_t)(part * 2 + t) * kSlot + r;
+#pragma unroll
+  for (int c = 0; c < G::DP; c += 16) {
+    uint32_t o[16];
+    tmem_ld16(tO + c, o);
+    tmem_wait_ld();
+    reg_fence(o, 0, 16);
+    if (c < D) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        if (c + e < D) __stcg(mine + (size_t)(c + e) * kBlockM, __uint_as_float(o[e]));
+    }
+  }
+  __stcg(mine + (size_t)G::DP * kBlockM, m);
+  __stcg(mine + (size_t)(G::DP + 1) * kBlockM, l);
+  int* cnt = counters + ((size_t)(2 * tail + t) * kBlockM + r);
+  if (atom_add_acq_rel_gpu(cnt, 1) != chunks - 1) return;
+  const float* first = parts + (size_t)(part0 * 2 + t) * kSlot + r;
+  const size_t cstride = 2 * kSlot;  // next chunk, same tile and row
+  auto mval = [&](int cc) -> float {
+    return cc < chunks ? __ldcg(first + cc * cstride + (size_t)G::DP * kBlockM) : -INFINITY;
+  };
+  auto lval = [&](int cc) -> float {
+    return cc < chunks ? __ldcg(first + cc * cstride + (size_t)(G::DP + 1) * kBlockM) : 0.f;
+  };
+  float mm = -INFINITY;
+  for (int cc = 0; cc < chunks; cc += 4)
+    mm = fmaxf(fmaxf(mm, fmaxf(mval(cc), mval(cc + 1))), fmaxf(mval(cc + 2), mval(cc + 3)));
+  float ll = 0.f;
+  for (int cc = 0; cc < chunks; cc += 4) {
+    float a[4], b[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      a[e] = mval(cc + e);
+      b[e] = lval(cc + e);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) ll += cc + e < chunks ? ex2(a[e] - mm) * b[e] : 0.f;
+  }
+  const float inv_l = 1.0f / ll;
+  // O in blocks of columns; one chunk's block per pass, its loads independent
+  constexpr int BC = D == 72 ? 24 : 32;
+  static_assert(D % BC == 0 && BC % 8 == 0, "merge blocks");
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += BC) {
+    float acc[BC];
+#pragma unroll
+    for (int e = 0; e < BC; ++e) acc[e] = 0.f;
+    for (int cc = 0; cc < chunks; ++cc) {
+      const float* src = first + cc * cstride + (size_t)c0 * kBlockM;
+      float v[BC];
+#pragma unroll
+      for (int e = 0; e < BC; ++e) v[e] = __ldcg(src + (size_t)e * kBlockM);
+      const float w = ex2(mval(cc) - mm);
+#pragma unroll
+      for (int e = 0; e < BC; ++e) acc[e] += w * v[e];
+    }
+    if (valid) {
+#pragma unroll
+      for (int e = 0; e < BC; e += 8)
+        *reinterpret_cast<uint4*>(orow + c0 + e) = make_uint4(
+            pack_bf16x2(acc[e] * inv_l, acc[e + 1] * inv_l),
+            pack_bf16x2(acc[e + 2] * inv_l, acc[e + 3] * inv_l),
+            pack_bf16x2(acc[e + 4] * inv_l, acc[e + 5] * inv_l),
+            pack_bf16x2(acc[e + 6] * inv_l, acc[e + 7] * inv_l));
+    }
+  }
+  *cnt = 0;  // ready for the next call
 }
 
 // -------------------------------------------------------------------- fwd
@@ -346,6 +558,20 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
   auto bar = [&](int i) -> uint32_t { return base + G::BAR_OFF + 8u * (uint32_t)i; };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base_ptr + G::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + G::MISC_OFF + 4);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(base_ptr + G::MISC_OFF + 8);
+  // Consumer side of the item ring (MMA issuers, softmax warps): the k-th
+  // item of this CTA, or -1 if a wait gave up.  Lane 0 of every consumer
+  // warp releases the entry once the warp has read it.
+  auto next_item = [&](int k) -> int {
+    const uint32_t islot = k % kItemDepth, iuse = k / kItemDepth;
+    const bool w = wait_bounded(bar(G::B_ITEM_FULL + islot), iuse & 1u, abort_flag, p.status,
+                                kStatusTimeoutItem);
+    if (!__all_sync(0xffffffffu, w)) return -1;
+    const int u = item_ring[islot];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar(G::B_ITEM_EMPTY + islot));
+    return u;
+  };
 
   // warp index made warp-uniform for the compiler (role branches below)
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
@@ -365,6 +591,10 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
     }
     mbar_init(bar(G::B_DRAIN + 0), 1);
     mbar_init(bar(G::B_DRAIN + 1), 1);
+    for (int i = 0; i < kItemDepth; ++i) {
+      mbar_init(bar(G::B_ITEM_FULL + i), 1);
+      mbar_init(bar(G::B_ITEM_EMPTY + i), G::ITEM_CONSUMERS);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -379,6 +609,10 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
 
   const WsLayout L = ws_layout(p.num_seqs);
   const int num_units = reinterpret_cast<const int*>(p.ws)[1];
+  const int num_items = reinterpret_cast<const int*>(p.ws)[2];
+  const int split_start = reinterpret_cast<const int*>(p.ws)[3];
+  const SplitLayout SL = split_layout(p.split_cap);
+  const int32_t* tail_prefix = reinterpret_cast<const int32_t*>(p.split + SL.prefix);
   const int32_t* order = reinterpret_cast<const int32_t*>(p.ws + L.order);
   const int32_t* prefix = reinterpret_cast<const int32_t*>(p.ws + L.prefix);
 
@@ -394,8 +628,25 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       return __all_sync(0xffffffffu,
                         wait_bounded(b, parity, abort_flag, p.status, kStatusTimeoutLoad));
     };
-    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-      const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, G::KN);
+    // Items are handed out dynamically, longest first: the CTA's first item
+    // is blockIdx.x, every later one comes from the workspace counter.  The
+    // producer publishes each item (or a past-the-end index) in the ring.
+    // The counter is read one item ahead, so its round trip overlaps the
+    // current item's loads.
+    const int leader_lane = __ffs(__ballot_sync(0xffffffffu, leader != 0)) - 1;
+    int pending = 0;
+    for (int k = 0; ok; ++k) {
+      const int u = k == 0 ? (int)blockIdx.x
+                           : (int)gridDim.x + __shfl_sync(0xffffffffu, pending, leader_lane);
+      const uint32_t islot = k % kItemDepth, iuse = k / kItemDepth;
+      if (!(ok = wait_(bar(G::B_ITEM_EMPTY + islot), (iuse & 1u) ^ 1u))) break;
+      if (leader) item_ring[islot] = u;
+      __syncwarp();
+      if (leader) mbar_arrive(bar(G::B_ITEM_FULL + islot));
+      if (u >= num_items) break;
+      if (leader) pending = atomicAdd(p.status + kHdrNextItem, 1);
+      const UnitInfo ui = decode_item(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, G::KN,
+                                        split_start, num_units, tail_prefix);
       if (ui.nkv == 0) continue;
       const uint8_t* mq = p.ws + L.maps + (size_t)ui.seq * kMapsPerSeq * kMapBytes;
       const uint8_t* mk = mq + kMapBytes;
@@ -431,7 +682,7 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
 #pragma unroll
         for (int b = 0; b < G::NB; ++b)
           tma_load_3d_if(leader, dst + b * G::KV_BOX_BYTES, m, bar(G::B_KV_FULL + stage),
-                         b * G::BW, ui.head, j * G::KN);
+                         b * G::BW, ui.head, (ui.jb + j) * G::KN);
         ++kv_item;
       }
     }
@@ -504,8 +755,11 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       return wait_(bar(G::B_KV_FULL + it % G::STAGES), (it / G::STAGES) & 1u);
     };
 
-    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-      const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, G::KN);
+    for (int k = 0; ok; ++k) {
+      const int u = next_item(k);
+      if (u < 0 || u >= num_items) break;
+      const UnitInfo ui = decode_item(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, G::KN,
+                                        split_start, num_units, tail_prefix);
       if (ui.nkv == 0) continue;
       if (!(ok = wait_(bar(G::B_Q_FULL), q_use & 1u))) break;
       ++q_use;
@@ -643,8 +897,11 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       return __all_sync(0xffffffffu, w);
     };
 
-    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-      const UnitInfo ui = decode_unit(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, KN);
+    for (int k = 0; ok; ++k) {
+      const int u = next_item(k);
+      if (u < 0 || u >= num_items) break;
+      const UnitInfo ui = decode_item(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, KN,
+                                        split_start, num_units, tail_prefix);
       if (t == 1 && !ui.t1) continue;
       const int row = ui.q0 + kBlockM * t + r;
       const bool valid = row < ui.lq;
@@ -664,7 +921,7 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
         tc_fence_after();
         uint32_t s[KN];
         // keys past the end of the sequence in its last tile
-        const int lim = ui.lk - j * KN;
+        const int lim = ui.lk - (ui.jb + j) * KN;
         const bool tail = lim < KN;  // only the last key tile can be partial
         tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
@@ -792,6 +1049,11 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       // epilogue: O / l -> bf16 -> out (rows of this sequence only)
       if (!(ok = wait_(bar(G::B_PV_DONE + t), (p_cnt - 1) & 1u))) break;
       tc_fence_after();
+      if (ui.part >= 0) {
+        split_epilogue<D>(p.split + SL.parts, reinterpret_cast<int*>(p.split + SL.counters), tO, t,
+                          r, m, l, orow, valid, ui.part, ui.part0, ui.tail, ui.chunks);
+        continue;
+      }
       const float inv = 1.0f / l;
 #pragma unroll
       for (int c = 0; c < G::DP; c += 16) {

@@ -304,6 +304,20 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_if(uint32_t leader, uint32
       : "memory");
 }
 
+// Barrier `id` (1-15) over `nthreads` threads of the CTA (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Atomic add at GPU scope with acquire-release order: earlier writes of this
+// thread are visible to whoever observes the new count, and writes made
+// visible by earlier adds are visible to this thread afterwards.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // ------------------------------------------------------------------- math
 __device__ __forceinline__ float ex2(float x) {
   float y;
