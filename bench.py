@@ -37,6 +37,8 @@ METRIC = "varlen attn fwd TFLOP/s (4*sum(L^2)*H*D)"
 PAGE_TPROD_TFLOPS = {  # the page's T_Prod converted with the same FLOP count
     C1.name: 2.0, C2.name: 80.5, C3.name: 123.1, C4.name: 83.3}
 L2_FLUSH_BYTES = 256 << 20
+NOMINAL_BF16_TFLOPS = 2250.0  # GB300 dense bf16, nominal (context; the roofline uses the measured peak)
+GRAPH_CALLS = 20              # calls per CUDA-graph replay for the launch-bound workload
 
 
 def kernel_source_sha() -> str:
@@ -221,6 +223,33 @@ def time_calls(fn, steps, flush_buf, stream):
     return [a.elapsed_time(b) for a, b in durs]
 
 
+def graph_us_per_call(fn, stream) -> float:
+    """Microseconds per call of `fn` replayed GRAPH_CALLS times from one
+    captured CUDA graph (launch overhead amortised); L2 stays warm."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(GRAPH_CALLS):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    reps = []
+    for _ in range(5):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        reps.append(a.elapsed_time(b) * 1e3 / GRAPH_CALLS)
+    return statistics.median(reps)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -292,7 +321,9 @@ def run_ours(args, rank, world, local_rank):
     e2e_value = whole_job_throughput(flops, e2e_steps, world,
                                      max_over_ranks(sum(e2e_durs) / 1e3, dev))
 
-    # every workload once more: microseconds per call and TFLOP/s
+    # every workload once more: microseconds per call with L2 flushed before
+    # each call (cold) and without (warm), TFLOP/s of the cold time; for the
+    # launch-bound C1 also the time per call inside a replayed CUDA graph
     shapes = {}
     if not args.headline_only:
         for ws in (C1, C2, C3, C4, C5):
@@ -302,18 +333,24 @@ def run_ours(args, rank, world, local_rank):
             for _ in range(3):
                 fn()
             n = 5 if ws is C4 else 20
-            d = time_calls(fn, n, flush, stream)
-            us = statistics.median(d) * 1e3
+            us = statistics.median(time_calls(fn, n, flush, stream)) * 1e3
+            us_warm = statistics.median(time_calls(fn, n, None, stream)) * 1e3
             tf = ws.flops() / (us * 1e-6) / 1e12
-            shapes[ws.name] = {"us": round(us, 2), "tflops": round(tf, 2),
-                               "pct_bf16_peak": round(100.0 * tf / peaks["bf16_tflops"], 2),
-                               "page_tprod_tflops": PAGE_TPROD_TFLOPS.get(ws.name)}
+            entry = {"us": round(us, 2), "us_warm_l2": round(us_warm, 2), "tflops": round(tf, 2),
+                     "pct_bf16_peak": round(100.0 * tf / peaks["bf16_tflops"], 2),
+                     "pct_nominal_2250": round(100.0 * tf / NOMINAL_BF16_TFLOPS, 2),
+                     "gbs_algorithmic": round(ws.algorithmic_bytes() / (us * 1e-6) / 1e9, 1),
+                     "page_tprod_tflops": PAGE_TPROD_TFLOPS.get(ws.name)}
+            if ws is C1:
+                entry["us_per_call_in_graph"] = round(graph_us_per_call(fn, stream), 2)
+            shapes[ws.name] = entry
             del ts, os_
         vlp.check()
 
     if rank != 0:
         return
     cpu = cpu_oracle_rate(w, max_seconds=args.cpu_seconds)
+    cpu1 = cpu_oracle_rate(w, max_seconds=min(4.0, args.cpu_seconds), nthreads=1)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -331,6 +368,7 @@ def run_ours(args, rank, world, local_rank):
                      "kernel": "attn_varlen_fwd_kernel<72> (+ plan kernel in the timed call)"},
         "cpu_baseline": {"value": cpu["tflops"], "unit": "TFLOP/s", "cores": cpu["cores"],
                          "kind": "oracle", "rows_per_s": cpu["rows_per_s"],
+                         "rows_per_s_1_thread": cpu1["rows_per_s"],
                          "sample": f"{cpu['rows']} seeded (token, head) rows of {w.name}, "
                                    f"all keys each, {cpu['seconds']:.1f} s"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

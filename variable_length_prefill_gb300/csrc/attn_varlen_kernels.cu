@@ -285,6 +285,9 @@ __device__ __forceinline__ bool kv_item_tile(int i, int n, int& j) {
 
 // ------------------------------------------------------------------- plan
 __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_constant__ PlanParams p) {
+  // the attention kernel may start launching now; it waits for this grid to
+  // complete before it reads the workspace
+  grid_launch_dependents();
   __shared__ int s_key[kLptMaxSeqs];
   __shared__ int s_warp[32];
   __shared__ int s_carry;
@@ -607,6 +610,8 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // everything above overlaps the plan kernel; the workspace is read below
+  grid_wait_prerequisite();
   const WsLayout L = ws_layout(p.num_seqs);
   const int num_units = reinterpret_cast<const int*>(p.ws)[1];
   const int num_items = reinterpret_cast<const int*>(p.ws)[2];
@@ -1089,10 +1094,21 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// Launched as a programmatic dependent of the plan kernel: its CTAs start
+// (barrier init, TMEM allocation) while the plan kernel still runs.
 template <int D>
 static cudaError_t launch_fwd_t(const FwdParams& p, int grid, cudaStream_t stream) {
-  attn_varlen_fwd_kernel<D><<<grid, Geometry<D>::THREADS, Geometry<D>::SMEM_BYTES, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)Geometry<D>::THREADS);
+  cfg.dynamicSmemBytes = Geometry<D>::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_varlen_fwd_kernel<D>, p);
 }
 
 cudaError_t prepare_fwd(int head_dim) {

@@ -318,6 +318,16 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
   return old;
 }
 
+// Programmatic dependent launch: the running grid lets the next grid on the
+// stream start launching; the dependent grid waits for this grid to finish
+// and its memory to be visible before it reads what this grid wrote.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_wait_prerequisite() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- math
 __device__ __forceinline__ float ex2(float x) {
   float y;
