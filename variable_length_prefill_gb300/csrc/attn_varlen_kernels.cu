@@ -91,8 +91,13 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 constexpr int kMergeTiles = 8;
 
 
-#ifndef ATTN_VARLEN_KV_STAGES
-#define ATTN_VARLEN_KV_STAGES 4
+// K/V ring depth per head_dim (shared memory: head_dim 72 holds 2 x 32 KB of
+// Q and 28 KB per stage, head_dim 128 2 x 32 KB and 32 KB per stage)
+#ifndef ATTN_VARLEN_KV_STAGES_72
+#define ATTN_VARLEN_KV_STAGES_72 4
+#endif
+#ifndef ATTN_VARLEN_KV_STAGES_128
+#define ATTN_VARLEN_KV_STAGES_128 4
 #endif
 
 template <int D>
@@ -105,7 +110,7 @@ struct Cfg<72> {
   static constexpr int KN = 112;   // keys per K/V tile
   static constexpr bool PSEP = true;  // P in TMEM columns of its own
   static constexpr int ISSUERS = 2;   // one MMA-issuing warp per Q tile
-  static constexpr int STAGES = ATTN_VARLEN_KV_STAGES;
+  static constexpr int STAGES = ATTN_VARLEN_KV_STAGES_72;
   static constexpr uint32_t SWZ = kSwizzle128B;
 };
 template <>
@@ -115,7 +120,7 @@ struct Cfg<128> {
   static constexpr int KN = 128;
   static constexpr bool PSEP = false;  // P overwrites the first half of S
   static constexpr int ISSUERS = 1;    // one MMA-issuing warp for both Q tiles
-  static constexpr int STAGES = ATTN_VARLEN_KV_STAGES;
+  static constexpr int STAGES = ATTN_VARLEN_KV_STAGES_128;
   static constexpr uint32_t SWZ = kSwizzle128B;
 };
 
@@ -289,6 +294,13 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
   // complete before it reads the workspace
   grid_launch_dependents();
   __shared__ int s_key[kLptMaxSeqs];
+  // with at most kLptMaxSeqs sequences the per-sequence lengths, the order
+  // and the prefix sums stay in shared memory, so the plan costs one round
+  // of global loads (the global copies are written for the attention kernel)
+  __shared__ int s_lq[kLptMaxSeqs];
+  __shared__ int s_lk[kLptMaxSeqs];
+  __shared__ int s_order[kLptMaxSeqs];
+  __shared__ int s_pref[kLptMaxSeqs + 1];
   __shared__ int s_warp[32];
   __shared__ int s_carry;
   const int N = p.num_seqs;
@@ -298,14 +310,26 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
   int* prefix = reinterpret_cast<int*>(p.ws + L.prefix);
   const bool lpt = N <= kLptMaxSeqs;
   const int tid = threadIdx.x, nt = blockDim.x;
+  auto lq_of = [&](int i) { return lpt ? s_lq[i] : p.cu_q[i + 1] - p.cu_q[i]; };
+  auto lk_of = [&](int i) { return lpt ? s_lk[i] : p.cu_k[i + 1] - p.cu_k[i]; };
+  auto order_at = [&](int r) { return lpt ? s_order[r] : order[r]; };
+  auto prefix_at = [&](int r) { return lpt ? s_pref[r] : prefix[r]; };
+  auto units_of = [&](int i) {
+    const int lq = lq_of(i);
+    return lq > 0 ? p.num_heads * ((lq + kUnitRows - 1) / kUnitRows) : 0;
+  };
 
-  // 1. per sequence: sort key, tensor maps
+  // 1. per sequence: lengths, sort key, tensor maps
   bool wrote_map = false;
   for (int i = tid; i < N; i += nt) {
     const int q0 = p.cu_q[i], lq = p.cu_q[i + 1] - q0;
     const int k0 = p.cu_k[i], lk = p.cu_k[i + 1] - k0;
     const bool live = lq > 0;
-    if (lpt) s_key[i] = live ? (lk > 0 ? lk : 0) : -1;
+    if (lpt) {
+      s_lq[i] = lq;
+      s_lk[i] = lk;
+      s_key[i] = live ? (lk > 0 ? lk : 0) : -1;
+    }
     if (live && lk > 0) {
       for (int m = 0; m < kMapsPerSeq; ++m) {
         uint8_t* dst = p.ws + L.maps + ((size_t)i * kMapsPerSeq + m) * kMapBytes;
@@ -335,6 +359,7 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
         const int kj = s_key[j];
         rank += (kj > ki) || (kj == ki && j < i);
       }
+      s_order[rank] = i;
     }
     order[rank] = i;
   }
@@ -344,11 +369,7 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
   const int chunk = (N + nt - 1) / nt;
   const int r0 = tid * chunk, r1 = min(N, r0 + chunk);
   int local = 0;
-  for (int r = r0; r < r1; ++r) {
-    const int i = order[r];
-    const int lq = p.cu_q[i + 1] - p.cu_q[i];
-    local += lq > 0 ? p.num_heads * ((lq + kUnitRows - 1) / kUnitRows) : 0;
-  }
+  for (int r = r0; r < r1; ++r) local += units_of(order_at(r));
   // block-wide exclusive scan of `local`
   const int lane = tid & 31, warp = tid >> 5;
   int incl = local;
@@ -375,11 +396,13 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
   int run = s_warp[warp] + incl - local;
   for (int r = r0; r < r1; ++r) {
     prefix[r] = run;
-    const int i = order[r];
-    const int lq = p.cu_q[i + 1] - p.cu_q[i];
-    run += lq > 0 ? p.num_heads * ((lq + kUnitRows - 1) / kUnitRows) : 0;
+    if (lpt) s_pref[r] = run;
+    run += units_of(order_at(r));
   }
-  if (tid == 0) prefix[N] = s_carry;
+  if (tid == 0) {
+    prefix[N] = s_carry;
+    if (lpt) s_pref[N] = s_carry;
+  }
   __syncthreads();
 
   // 4. tail split: the units of the last, partial wave of the persistent
@@ -395,10 +418,9 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
   const int t0 = U - R;  // first tail unit
   if (try_split) {
     for (int r = tid; r < N; r += nt) {
-      const int ua = max(prefix[r], t0), ub = prefix[r + 1];
+      const int ua = max(prefix_at(r), t0), ub = prefix_at(r + 1);
       if (ua < ub) {
-        const int sq = order[r];
-        const int lk = p.cu_k[sq + 1] - p.cu_k[sq];
+        const int lk = lk_of(order_at(r));
         const int nkv = lk > 0 ? (lk + p.kv_rows - 1) / p.kv_rows : 0;
         for (int u = ua; u < ub; ++u) s_key[u - t0] = nkv;
       }
