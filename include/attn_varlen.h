@@ -44,7 +44,7 @@ extern "C" {
 /* Return codes. */
 #define ATTN_VARLEN_OK                     0
 #define ATTN_VARLEN_ERR_INVALID_ARG       -1  /* null pointer, negative count, ... */
-#define ATTN_VARLEN_ERR_UNSUPPORTED_DIM   -2  /* head_dim not 72 or 128            */
+#define ATTN_VARLEN_ERR_UNSUPPORTED_DIM   -2  /* head_dim not 64, 72, 80, 96, 128  */
 #define ATTN_VARLEN_ERR_MISALIGNED        -3  /* q, k, v or out not 16-byte aligned */
 #define ATTN_VARLEN_ERR_UNSUPPORTED_DEVICE -4 /* current device is not sm_103       */
 #define ATTN_VARLEN_ERR_CUDA              -5  /* a CUDA runtime call failed         */
@@ -62,14 +62,19 @@ extern "C" {
  *   cu_seqlens_k  int32 device array [num_seqs + 1]
  *   num_seqs      >= 0; 0 returns ATTN_VARLEN_OK without launching anything
  *   num_heads     >= 1 (query, key and value heads are the same count)
- *   head_dim      72 or 128
+ *   head_dim      64, 72, 80, 96 or 128.  The page's shapes use 72 and 128; 72
+ *                 runs padded to 80 (zero columns add nothing to Q.K^T), and 64,
+ *                 80 and 96 run on the same schedule, always scaled by the true
+ *                 head_dim
  *   out           bf16 device buffer [total_q, num_heads, head_dim], 16-byte
  *                 aligned; must not overlap q, k or v
  *   stream        CUDA stream the work is queued on (0 = legacy default)
  *
- * Uses a workspace that the library owns, one per device, sized by num_seqs.
- * When it must grow, the call synchronises the device once to free the old
- * one.  Calls that share a device must be ordered (same stream, or
+ * Uses a workspace that the library owns, one per device, sized by num_seqs
+ * plus a region, sized by the SM count, in which the units of the grid's last
+ * partial wave may be split along the key range and merged (fp32 partials,
+ * merged in a fixed order, so results are deterministic).  When it must grow,
+ * the call synchronises the device once to free the old one.  Calls that share a device must be ordered (same stream, or
  * synchronised); concurrent calls on different streams must each pass their
  * own workspace to attn_varlen_fwd_ws.  Errors detected inside the kernels
  * (a wait that timed out) are recorded in the workspace and reported by

@@ -28,6 +28,13 @@ SMALL = [
     # multiples, with one and two Q tiles
     ((200,), (111,), 2, 72), ((200,), (112,), 2, 72), ((129,), (113,), 2, 72),
     ((300,), (224,), 1, 72), ((257,), (225,), 2, 72), ((112, 113, 224), None, 2, 72),
+    # head_dim 64 (128-key tiles), 80 (112-key tiles) and 96 (96-key tiles)
+    ((1,), None, 2, 64), ((200,), (127,), 2, 64), ((129,), (129,), 2, 64),
+    ((5, 130, 0, 257, 1, 64), None, 3, 64), ((300,), (1000,), 2, 64),
+    ((1,), None, 2, 80), ((200,), (111,), 2, 80), ((257,), (113,), 2, 80),
+    ((5, 130, 0, 257, 1, 64), None, 3, 80), ((100, 300, 7), (257, 64, 1000), 2, 80),
+    ((1,), None, 2, 96), ((200,), (95,), 2, 96), ((129,), (97,), 2, 96), ((300,), (193,), 1, 96),
+    ((5, 130, 0, 257, 1, 64), None, 3, 96), ((100, 300, 7), (257, 64, 1000), 2, 96),
 ]
 
 
@@ -188,7 +195,7 @@ def test_caller_workspace_on_two_streams(cuda_lib):
 def test_errors_raise(cuda_lib):
     import torch
     from variable_length_prefill_gb300 import AttnVarlenError
-    q = torch.zeros(8, 2, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(8, 2, 48, dtype=torch.bfloat16, device="cuda")  # head_dim 48: not built
     cu = torch.tensor([0, 8], dtype=torch.int32, device="cuda")
     with pytest.raises(AttnVarlenError) as e:
         cuda_lib.attn_varlen_fwd(q, q, q, cu, cu)
@@ -241,3 +248,10 @@ def test_tail_split_mixed_batch(cuda_lib):
     absv = oracle.attn_varlen(x["q"], x["k"], abs_bits(x["v"]), x["cu_q"], x["cu_k"])
     assert_close(got[live], ref[live], "tail_mixed caller workspace",
                  bound=bf16_bound(ref[live], absv[live]))
+
+
+@pytest.mark.parametrize("D", [64, 80, 96])
+def test_other_head_dims_sampled(cuda_lib, D):
+    """A longer sequence at every extra head_dim: 512 rows per head."""
+    w = Workload(f"L4500_H8_D{D}", (4500,), 8, D, seed=50 + D)
+    check_sampled(cuda_lib, w, 512)

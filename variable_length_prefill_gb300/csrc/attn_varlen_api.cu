@@ -21,7 +21,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool probed = false;
   bool supported = false;
-  bool prepared[2] = {false, false};  // kernel attributes for head_dim 72, 128
+  bool prepared[129] = {};  // kernel attributes set, by head_dim
   int sm_count = 0;
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -82,7 +82,7 @@ int get_encoder() {
 int check_args(const void* q, const void* k, const void* v, const int32_t* cu_q,
                const int32_t* cu_k, int num_seqs, int num_heads, int head_dim, const void* out) {
   if (num_seqs < 0 || num_heads < 1) return ATTN_VARLEN_ERR_INVALID_ARG;
-  if (head_dim != 72 && head_dim != 128) return ATTN_VARLEN_ERR_UNSUPPORTED_DIM;
+  if (!avp::head_dim_supported(head_dim)) return ATTN_VARLEN_ERR_UNSUPPORTED_DIM;
   if (num_seqs == 0) return ATTN_VARLEN_OK;
   if (!q || !k || !v || !cu_q || !cu_k || !out) return ATTN_VARLEN_ERR_INVALID_ARG;
   const uintptr_t mis = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
@@ -173,7 +173,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const 
   fp.num_heads = num_heads;
   fp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
 
-  const int slot = head_dim == 72 ? 0 : 1;
+  const int slot = head_dim;
   if (!st.prepared[slot]) {
     cudaError_t pe = avp::prepare_fwd(head_dim);
     if (pe != cudaSuccess) return fail_cuda(pe);
@@ -337,7 +337,7 @@ const char* attn_varlen_strerror(int code) {
   switch (code) {
     case ATTN_VARLEN_OK: return "ok";
     case ATTN_VARLEN_ERR_INVALID_ARG: return "invalid argument";
-    case ATTN_VARLEN_ERR_UNSUPPORTED_DIM: return "head_dim must be 72 or 128";
+    case ATTN_VARLEN_ERR_UNSUPPORTED_DIM: return "head_dim must be 64, 72, 80, 96 or 128";
     case ATTN_VARLEN_ERR_MISALIGNED: return "q, k, v and out must be 16-byte aligned (cu_seqlens 4-byte)";
     case ATTN_VARLEN_ERR_UNSUPPORTED_DEVICE: return "current device is not sm_103 (GB300)";
     case ATTN_VARLEN_ERR_CUDA: return "CUDA runtime error";

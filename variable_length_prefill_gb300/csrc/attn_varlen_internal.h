@@ -122,7 +122,8 @@ struct FwdParams {
 
 // Kernel launchers (attn_varlen_kernels.cu).
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
-cudaError_t prepare_fwd(int head_dim);  // per device, before the first launch
+bool head_dim_supported(int head_dim);  // 64, 72, 80, 96, 128
+cudaError_t prepare_fwd(int head_dim);  // per device and head_dim, before the first launch
 cudaError_t launch_fwd(int head_dim, const FwdParams& p, int grid, cudaStream_t stream);
 int fwd_threads(int head_dim);
 size_t fwd_smem_bytes(int head_dim);

@@ -61,6 +61,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "attn_varlen_internal.h"
 #include "ptx.cuh"
@@ -100,8 +101,42 @@ constexpr int kMergeTiles = 8;
 #define ATTN_VARLEN_KV_STAGES_128 4
 #endif
 
+// Per head_dim configuration.  Every head_dim other than 128 runs the
+// separate-P, two-issuer schedule; the key tile is the largest multiple of 16
+// whose S, P and O columns for two Q tiles fit the 512 TMEM columns
+// (2 KN + 2 KN/2 + 2 DP <= 512, with P placed at 2 KN + 64 t).
 template <int D>
 struct Cfg;
+template <>
+struct Cfg<64> {
+  static constexpr int DP = 64;
+  static constexpr int BW = 64;    // one 64-column box
+  static constexpr int KN = 128;
+  static constexpr bool PSEP = true;
+  static constexpr int ISSUERS = 2;
+  static constexpr int STAGES = 6;  // 16 KB per K or V tile
+  static constexpr uint32_t SWZ = kSwizzle128B;
+};
+template <>
+struct Cfg<80> {
+  static constexpr int DP = 80;
+  static constexpr int BW = 64;    // second box: columns 64-79 and zero fill
+  static constexpr int KN = 112;
+  static constexpr bool PSEP = true;
+  static constexpr int ISSUERS = 2;
+  static constexpr int STAGES = 4;
+  static constexpr uint32_t SWZ = kSwizzle128B;
+};
+template <>
+struct Cfg<96> {
+  static constexpr int DP = 96;
+  static constexpr int BW = 64;    // second box: columns 64-95 and zero fill
+  static constexpr int KN = 96;
+  static constexpr bool PSEP = true;
+  static constexpr int ISSUERS = 2;
+  static constexpr int STAGES = 4;
+  static constexpr uint32_t SWZ = kSwizzle128B;
+};
 template <>
 struct Cfg<72> {
   static constexpr int DP = 80;    // padded head_dim (MMA K and N multiple of 16)
@@ -159,7 +194,8 @@ struct Geometry {
   static_assert(SMEM_BYTES <= 232448, "shared memory above the sm_103 per-block limit");
   static constexpr int NK_S = DP / 16;  // K-steps of S = Q K^T
   static constexpr int NK_PV = KN / 16; // K-steps of O += P V
-  static_assert(KN % 16 == 0 && KN >= 64 && KN <= 128, "key tile rows");
+  static_assert(KN % 32 == 0 || KN == 112, "key tile rows: 64, 96, 112 or 128");
+  static_assert(KN >= 64 && KN <= 128, "key tile rows");
   static_assert(DP + 2 <= kPartRowMax, "partial row");
   // TMEM columns of S_t, P_t (bf16 pairs) and O_t
   __host__ __device__ static constexpr uint32_t s_col(int t) { return PSEP ? (uint32_t)(t * KN) : 128u * t; }
@@ -540,7 +576,7 @@ __device__ __noinline__ void split_epilogue(uint8_t* parts_base, int* counters, 
   }
   const float inv_l = 1.0f / ll;
   // O in blocks of columns; one chunk's block per pass, its loads independent
-  constexpr int BC = D == 72 ? 24 : 32;
+  constexpr int BC = D % 32 == 0 ? 32 : (D % 24 == 0 ? 24 : 40);
   static_assert(D % BC == 0 && BC % 8 == 0, "merge blocks");
 #pragma unroll 1
   for (int c0 = 0; c0 < D; c0 += BC) {
@@ -954,11 +990,9 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
         tmem_wait_ld();
         reg_fence(s, 0, 64);
-        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-        if constexpr (KN == 128)
-          tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-        else
-          tmem_ld16(tS + 96, *reinterpret_cast<uint32_t(*)[16]>(&s[96]));
+        if constexpr (KN >= 96) tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+        if constexpr (KN == 112) tmem_ld16(tS + 96, *reinterpret_cast<uint32_t(*)[16]>(&s[96]));
+        if constexpr (KN == 128) tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
         float mx0, mx1, mx2, mx3;
         if (!tail) {
           // row max of the first 64 keys while the rest is in flight
@@ -1054,10 +1088,14 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
           // P_t(j-1) must have been read by its P.V before it is overwritten
           if (p_cnt > 0 && !(ok = wait_(bar(G::B_PV_DONE + t), (p_cnt - 1) & 1u))) break;
           tc_fence_after();
-          static_assert(KN == 112, "P store split below assumes 56 packed columns");
+          // KN / 2 packed columns: 32 + (16 | 16 + 8 | 32)
           tmem_st32(tP + 0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-          tmem_st16(tP + 32, *reinterpret_cast<const uint32_t(*)[16]>(&pk[32]));
-          tmem_st8(tP + 48, *reinterpret_cast<const uint32_t(*)[8]>(&pk[48]));
+          if constexpr (KN == 96 || KN == 112)
+            tmem_st16(tP + 32, *reinterpret_cast<const uint32_t(*)[16]>(&pk[32]));
+          if constexpr (KN == 112)
+            tmem_st8(tP + 48, *reinterpret_cast<const uint32_t(*)[8]>(&pk[48]));
+          if constexpr (KN == 128)
+            tmem_st32(tP + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
         } else {
           // P_t overwrites the first half of S_t, already in registers
 #pragma unroll
@@ -1133,38 +1171,57 @@ static cudaError_t launch_fwd_t(const FwdParams& p, int grid, cudaStream_t strea
   return cudaLaunchKernelEx(&cfg, attn_varlen_fwd_kernel<D>, p);
 }
 
+// head_dim dispatch: calls f(std::integral_constant<int, D>) for a built D.
+template <typename F>
+static auto with_head_dim(int head_dim, F&& f) -> decltype(f(std::integral_constant<int, 72>{})) {
+  switch (head_dim) {
+    case 64: return f(std::integral_constant<int, 64>{});
+    case 72: return f(std::integral_constant<int, 72>{});
+    case 80: return f(std::integral_constant<int, 80>{});
+    case 96: return f(std::integral_constant<int, 96>{});
+    default: return f(std::integral_constant<int, 128>{});
+  }
+}
+
+bool head_dim_supported(int head_dim) {
+  return head_dim == 64 || head_dim == 72 || head_dim == 80 || head_dim == 96 || head_dim == 128;
+}
+
 cudaError_t prepare_fwd(int head_dim) {
-  if (head_dim == 72)
-    return cudaFuncSetAttribute(attn_varlen_fwd_kernel<72>,
+  if (!head_dim_supported(head_dim)) return cudaErrorInvalidValue;
+  return with_head_dim(head_dim, [](auto d) {
+    constexpr int D = decltype(d)::value;
+    return cudaFuncSetAttribute(attn_varlen_fwd_kernel<D>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)Geometry<72>::SMEM_BYTES);
-  if (head_dim == 128)
-    return cudaFuncSetAttribute(attn_varlen_fwd_kernel<128>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)Geometry<128>::SMEM_BYTES);
-  return cudaErrorInvalidValue;
+                                (int)Geometry<D>::SMEM_BYTES);
+  });
 }
 
 cudaError_t launch_fwd(int head_dim, const FwdParams& p, int grid, cudaStream_t stream) {
-  if (head_dim == 72) return launch_fwd_t<72>(p, grid, stream);
-  if (head_dim == 128) return launch_fwd_t<128>(p, grid, stream);
-  return cudaErrorInvalidValue;
+  if (!head_dim_supported(head_dim)) return cudaErrorInvalidValue;
+  return with_head_dim(head_dim, [&](auto d) { return launch_fwd_t<decltype(d)::value>(p, grid, stream); });
 }
 
 int fwd_threads(int head_dim) {
-  return head_dim == 72 ? Geometry<72>::THREADS : Geometry<128>::THREADS;
+  return with_head_dim(head_dim, [](auto d) { return Geometry<decltype(d)::value>::THREADS; });
 }
 
 size_t fwd_smem_bytes(int head_dim) {
-  return head_dim == 72 ? Geometry<72>::SMEM_BYTES : Geometry<128>::SMEM_BYTES;
+  return with_head_dim(head_dim,
+                       [](auto d) { return (size_t)Geometry<decltype(d)::value>::SMEM_BYTES; });
 }
 
-int box_cols(int head_dim) { return head_dim == 72 ? Cfg<72>::BW : Cfg<128>::BW; }
+int box_cols(int head_dim) {
+  return with_head_dim(head_dim, [](auto d) { return Cfg<decltype(d)::value>::BW; });
+}
 
-int kv_tile_rows(int head_dim) { return head_dim == 72 ? Cfg<72>::KN : Cfg<128>::KN; }
+int kv_tile_rows(int head_dim) {
+  return with_head_dim(head_dim, [](auto d) { return Cfg<decltype(d)::value>::KN; });
+}
 
 bool box_swizzle_128(int head_dim) {
-  return (head_dim == 72 ? Cfg<72>::SWZ : Cfg<128>::SWZ) == kSwizzle128B;
+  return with_head_dim(head_dim,
+                       [](auto d) { return Cfg<decltype(d)::value>::SWZ == kSwizzle128B; });
 }
 
 }  // namespace avp
