@@ -54,9 +54,9 @@ def _lib(mutation: int = 0):
             lib = ctypes.CDLL(build(mutation))
             p = ctypes.c_void_p
             i = ctypes.c_int
-            lib.oracle_attn_varlen.argtypes = [p, p, p, p, p, i, i, i, p, i]
+            lib.oracle_attn_varlen.argtypes = [p, p, p, p, p, i, i, i, i, p, i]
             lib.oracle_attn_varlen.restype = i
-            lib.oracle_attn_rows.argtypes = [p, p, p, p, p, i, i, i, p,
+            lib.oracle_attn_rows.argtypes = [p, p, p, p, p, i, i, i, i, p,
                                              ctypes.c_int64, p, i]
             lib.oracle_attn_rows.restype = i
             lib.oracle_max_threads.argtypes = [i]
@@ -86,25 +86,27 @@ def max_threads(nthreads: int = 0) -> int:
 
 
 def attn_varlen(q, k, v, cu_q, cu_k, nthreads: int = 0, mutation: int = 0,
-                fill: float = np.nan) -> np.ndarray:
+                fill: float = np.nan, causal: bool = False) -> np.ndarray:
     """All output rows, float64 [total_q, H, D].
 
     ``q, k, v`` are bf16 bit patterns (uint16) of shape [T, H, D].  Rows that
-    no non-empty query sequence covers keep ``fill``.
+    no non-empty query sequence covers keep ``fill``.  ``causal``: row r of a
+    sequence sees keys j <= r + L_k - L_q (bottom-right aligned mask).
     """
     q, k, v, cu_q, cu_k = _prep(q, k, v, cu_q, cu_k)
     T, H, D = q.shape
     out = np.full((T, H, D), fill, dtype=np.float64)
     rc = _lib(mutation).oracle_attn_varlen(
         q.ctypes.data, k.ctypes.data, v.ctypes.data, cu_q.ctypes.data,
-        cu_k.ctypes.data, cu_q.size - 1, H, D, out.ctypes.data, int(nthreads))
+        cu_k.ctypes.data, cu_q.size - 1, H, D, int(bool(causal)), out.ctypes.data,
+        int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_attn_varlen failed with {rc}")
     return out
 
 
 def attn_rows(q, k, v, cu_q, cu_k, rows, nthreads: int = 0,
-              mutation: int = 0) -> np.ndarray:
+              mutation: int = 0, causal: bool = False) -> np.ndarray:
     """Selected output rows, float64 [n, D]; ``rows`` is int [n, 2] of (token, head)."""
     q, k, v, cu_q, cu_k = _prep(q, k, v, cu_q, cu_k)
     T, H, D = q.shape
@@ -112,7 +114,7 @@ def attn_rows(q, k, v, cu_q, cu_k, rows, nthreads: int = 0,
     out = np.zeros((rows.shape[0], D), dtype=np.float64)
     rc = _lib(mutation).oracle_attn_rows(
         q.ctypes.data, k.ctypes.data, v.ctypes.data, cu_q.ctypes.data,
-        cu_k.ctypes.data, cu_q.size - 1, H, D, rows.ctypes.data,
+        cu_k.ctypes.data, cu_q.size - 1, H, D, int(bool(causal)), rows.ctypes.data,
         rows.shape[0], out.ctypes.data, int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_attn_rows failed with {rc}")

@@ -27,6 +27,14 @@
  * IEEE double with libm exp.  There is no tiling, no exp2 and no online
  * rescaling: the max is found first, then the weights, then the weighted sum.
  *
+ * Causal variant (not on the page, which is non-causal; offered as the
+ * common prefill neighbour): query row r of a sequence (0-based within its
+ * slice) sees only keys j <= r + (L_k - L_q), i.e. the mask is aligned to the
+ * bottom-right corner, so that the last query row sees every key (the
+ * convention of prefill after a cached prefix; for L_q = L_k it is the usual
+ * lower triangle).  A row that sees no key gets a zero row, like an empty key
+ * slice.
+ *
  * Readings where the page is silent:
  *  - a sequence with an empty (or negative) query slice is skipped, and its
  *    output rows are not written (the page's loop skips it);
@@ -44,6 +52,10 @@
 #include <omp.h>
 #endif
 
+/* Keys visible to row r (0-based in its query slice) of a sequence with Lq
+ * queries and Lk keys: all Lk, or with the causal mask min(Lk, r + 1 + Lk - Lq). */
+static int64_t visible_keys(int64_t r, int64_t Lq, int64_t Lk, int causal);
+
 /* Plant-a-mistake hook for the oracle's own pin tests: the tests build a
  * separate copy of this file with -DORACLE_MUTATION=n and check that the pins
  * catch each mistake.  The normal build defines nothing and every MUT(n) is 0. */
@@ -51,6 +63,16 @@
 #define ORACLE_MUTATION 0
 #endif
 #define MUT(n) (ORACLE_MUTATION == (n))
+
+static int64_t visible_keys(int64_t r, int64_t Lq, int64_t Lk, int causal) {
+    if (!causal) return Lk;
+    int64_t lim;
+    if (MUT(11)) lim = r + Lk - Lq;          /* planted: the diagonal key dropped */
+    else if (MUT(12)) lim = r + 1;           /* planted: top-left alignment */
+    else lim = r + 1 + Lk - Lq;
+    if (lim > Lk) lim = Lk;
+    return lim > 0 ? lim : 0;
+}
 
 static double bf16_to_double(uint16_t b) {
     uint32_t u = ((uint32_t)b) << 16;
@@ -126,7 +148,7 @@ int oracle_max_threads(int nthreads) {
  */
 int oracle_attn_varlen(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                        const int32_t* cu_q, const int32_t* cu_k, int num_seqs,
-                       int H, int D, double* out, int nthreads) {
+                       int H, int D, int causal, double* out, int nthreads) {
     if (num_seqs < 0 || H <= 0 || D <= 0) return -1;
     set_threads(nthreads);
     int err = 0;
@@ -148,7 +170,7 @@ int oracle_attn_varlen(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                 for (int64_t idx = 0; idx < n; ++idx) {
                     int64_t t = q0 + idx / H;
                     int h = (int)(idx % H);
-                    attend_row(q, k, v, t, k0, Lk, H, D, h,
+                    attend_row(q, k, v, t, k0, visible_keys(t - q0, Lq, Lk, causal), H, D, h,
                                out + t * (int64_t)H * D + (int64_t)h * D, s);
                 }
                 free(s);
@@ -165,7 +187,7 @@ int oracle_attn_varlen(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  */
 int oracle_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                      const int32_t* cu_q, const int32_t* cu_k, int num_seqs,
-                     int H, int D, const int64_t* rows, int64_t n_rows,
+                     int H, int D, int causal, const int64_t* rows, int64_t n_rows,
                      double* out, int nthreads) {
     if (num_seqs < 0 || H <= 0 || D <= 0 || n_rows < 0) return -1;
     set_threads(nthreads);
@@ -200,7 +222,9 @@ int oracle_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                 int64_t k0 = MUT(4) ? cu_q[found] : cu_k[found];
                 int64_t Lk = (int64_t)cu_k[found + 1] - cu_k[found];
                 if (Lk < 0) Lk = 0;
-                attend_row(q, k, v, t, k0, Lk, H, D, h, out + r * (int64_t)D, s);
+                const int64_t Lq = (int64_t)cu_q[found + 1] - cu_q[found];
+                attend_row(q, k, v, t, k0, visible_keys(t - cu_q[found], Lq, Lk, causal), H, D,
+                           h, out + r * (int64_t)D, s);
             }
             free(s);
         }

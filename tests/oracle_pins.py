@@ -261,7 +261,97 @@ def pin_rows_match_full(mutation=0):
     np.testing.assert_array_equal(part, full[rows[:, 0], rows[:, 1]])
 
 
+# ------------------------------------------------------------------ causal
+# The causal variant (not on the page; the common prefill neighbour): row r of
+# a sequence sees keys j <= r + L_k - L_q, a mask aligned to the bottom-right
+# corner; rows that see no key are zero.
+
+
+def _run_causal(q, k, v, cu_q, cu_k, mutation):
+    return oracle.attn_varlen(q, k, v, cu_q, cu_k, mutation=mutation, causal=True)
+
+
+def pin_causal_first_and_last_row(mutation=0):
+    """L_q = L_k: the first row sees one key, so it is that key's v row; the
+    last row sees every key, so it equals the non-causal row."""
+    rng = np.random.default_rng(40)
+    H, D = 2, 8
+    lens = [6, 1, 9]
+    q = _rand_bits(rng, (sum(lens), H, D))
+    k = _rand_bits(rng, (sum(lens), H, D))
+    v = _rand_bits(rng, (sum(lens), H, D))
+    cu = _cu(lens, offset=3)
+    q = np.concatenate([_rand_bits(rng, (3, H, D)), q])
+    k = np.concatenate([_rand_bits(rng, (3, H, D)), k])
+    v = np.concatenate([_rand_bits(rng, (3, H, D)), v])
+    causal = _run_causal(q, k, v, cu, cu, mutation)
+    full = _run(q, k, v, cu, cu, mutation)
+    vf = bf16_bits_to_f64(v)
+    for i in range(len(lens)):
+        first, last = cu[i], cu[i + 1] - 1
+        np.testing.assert_allclose(causal[first], vf[first], rtol=0, atol=1e-15)
+        np.testing.assert_allclose(causal[last], full[last], rtol=0, atol=1e-12)
+
+
+def pin_causal_torch_sdpa(mutation=0):
+    """L_q = L_k: torch's float64 SDPA with is_causal=True (lower triangle) is an
+    independent implementation; it must agree to 1e-10."""
+    import torch
+    rng = np.random.default_rng(41)
+    H, D = 3, 72
+    lens = [1, 17, 40, 5]
+    q = _rand_bits(rng, (sum(lens), H, D))
+    k = _rand_bits(rng, (sum(lens), H, D))
+    v = _rand_bits(rng, (sum(lens), H, D))
+    cu = _cu(lens)
+    out = _run_causal(q, k, v, cu, cu, mutation)
+    qf, kf, vf = (torch.from_numpy(bf16_bits_to_f64(x)) for x in (q, k, v))
+    for i in range(len(lens)):
+        sl = slice(cu[i], cu[i + 1])
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qf[sl].transpose(0, 1)[None], kf[sl].transpose(0, 1)[None],
+            vf[sl].transpose(0, 1)[None], is_causal=True)
+        np.testing.assert_allclose(out[sl], ref[0].transpose(0, 1).numpy(), rtol=0, atol=1e-10)
+
+
+def pin_causal_bottom_right(mutation=0):
+    """L_q != L_k: row r equals the non-causal result over the first
+    r + 1 + L_k - L_q keys (the mask's corner sits at the last query and the
+    last key); rows with no visible key are zero."""
+    rng = np.random.default_rng(42)
+    H, D = 2, 8
+    for lq, lk in ((5, 12), (9, 4)):
+        q = _rand_bits(rng, (lq, H, D))
+        k = _rand_bits(rng, (lk, H, D))
+        v = _rand_bits(rng, (lk, H, D))
+        out = _run_causal(q, k, v, _cu([lq]), _cu([lk]), mutation)
+        for r in range(lq):
+            n = min(lk, r + 1 + lk - lq)
+            if n <= 0:
+                np.testing.assert_array_equal(out[r], 0.0)
+                continue
+            one = _run(q[r:r + 1], k[:n], v[:n], _cu([1]), _cu([n]), mutation)
+            np.testing.assert_allclose(out[r], one[0], rtol=0, atol=1e-12)
+
+
+def pin_causal_rows_match_full(mutation=0):
+    """The sampled-rows entry point applies the same causal mask."""
+    rng = np.random.default_rng(43)
+    H, D = 2, 16
+    lens_q, lens_k = [4, 7, 3], [9, 7, 1]
+    q = _rand_bits(rng, (sum(lens_q), H, D))
+    k = _rand_bits(rng, (sum(lens_k), H, D))
+    v = _rand_bits(rng, (sum(lens_k), H, D))
+    cu_q, cu_k = _cu(lens_q), _cu(lens_k)
+    full = _run_causal(q, k, v, cu_q, cu_k, mutation)
+    rows = np.array([[0, 0], [3, 1], [4, 0], [10, 1], [11, 0], [12, 1], [13, 0]])
+    part = oracle.attn_rows(q, k, v, cu_q, cu_k, rows, mutation=mutation, causal=True)
+    np.testing.assert_array_equal(part, full[rows[:, 0], rows[:, 1]])
+
+
 PINS = [pin_single_key, pin_constant_keys, pin_zero_query, pin_equal_values,
         pin_two_keys, pin_key_permutation, pin_key_translation,
         pin_value_affine, pin_row_independence, pin_head_independence,
-        pin_packing, pin_empty_and_offsets, pin_torch_sdpa, pin_rows_match_full]
+        pin_packing, pin_empty_and_offsets, pin_torch_sdpa, pin_rows_match_full,
+        pin_causal_first_and_last_row, pin_causal_torch_sdpa, pin_causal_bottom_right,
+        pin_causal_rows_match_full]

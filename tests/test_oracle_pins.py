@@ -20,7 +20,8 @@ def test_pin(pin):
 #  4 keys located with the query offsets 5 head and dim indices swapped in K
 #  6 the last key dropped                7 V row of the query token
 #  9 sign of the exponent flipped       10 NaN instead of zeros for L_k = 0
-MUTATIONS = [1, 3, 4, 5, 6, 7, 9, 10]
+# 11 causal: the diagonal key dropped   12 causal: mask aligned top-left
+MUTATIONS = [1, 3, 4, 5, 6, 7, 9, 10, 11, 12]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS)
@@ -34,14 +35,17 @@ def test_planted_mistake_is_caught(mutation):
     assert failed, f"no pin catches planted mistake {mutation}"
 
 
-def _brute_force(q, k, v, cu_q, cu_k, H, D):
-    """Scalar triple loop in Python floats, for tiny inputs."""
+def _brute_force(q, k, v, cu_q, cu_k, H, D, causal=False):
+    """Scalar triple loop in Python floats, for tiny inputs.  ``causal``: row
+    r of a sequence sees keys j <= r + L_k - L_q."""
     qf, kf, vf = (bf16_bits_to_f64(x) for x in (q, k, v))
     out = {}
     for i in range(len(cu_q) - 1):
+        lq, lk = cu_q[i + 1] - cu_q[i], cu_k[i + 1] - cu_k[i]
         for r in range(cu_q[i], cu_q[i + 1]):
             for h in range(H):
-                ks = list(range(cu_k[i], cu_k[i + 1]))
+                ks = [j for j in range(cu_k[i], cu_k[i + 1])
+                      if not causal or (j - cu_k[i]) <= (r - cu_q[i]) + lk - lq]
                 if not ks:
                     out[(r, h)] = [0.0] * D
                     continue
@@ -55,18 +59,19 @@ def _brute_force(q, k, v, cu_q, cu_k, H, D):
     return out
 
 
+@pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("D", [4, 72, 128])
-def test_brute_force_tiny(D):
+def test_brute_force_tiny(D, causal):
     rng = np.random.default_rng(30 + D)
     from oracle_pins import _cu, _rand_bits
     H = 2
-    lens_q, lens_k = [1, 3, 0, 2], [2, 3, 4, 0]
+    lens_q, lens_k = [1, 3, 0, 2, 4, 3], [2, 3, 4, 0, 2, 5]
     q = _rand_bits(rng, (sum(lens_q), H, D))
     k = _rand_bits(rng, (sum(lens_k), H, D))
     v = _rand_bits(rng, (sum(lens_k), H, D))
     cu_q, cu_k = _cu(lens_q), _cu(lens_k)
-    out = oracle.attn_varlen(q, k, v, cu_q, cu_k)
-    ref = _brute_force(q, k, v, cu_q, cu_k, H, D)
+    out = oracle.attn_varlen(q, k, v, cu_q, cu_k, causal=causal)
+    ref = _brute_force(q, k, v, cu_q, cu_k, H, D, causal=causal)
     for (r, h), row in ref.items():
         np.testing.assert_allclose(out[r, h], row, rtol=0, atol=1e-12)
 
