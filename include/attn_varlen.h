@@ -85,6 +85,23 @@ int attn_varlen_fwd(const void* q, const void* k, const void* v,
                     int num_seqs, int num_heads, int head_dim,
                     void* out, cudaStream_t stream);
 
+/*
+ * attn_varlen_fwd_causal -- attn_varlen_fwd with a causal mask.  The page's
+ * operation is non-causal (its scaled_dot_product_attention call passes
+ * is_causal=False); this is the common prefill neighbour.  Row r of sequence
+ * i (0-based within its query slice) sees only the keys j <= r + L_k - L_q of
+ * that sequence: the mask is aligned to the bottom-right corner, so the last
+ * query row sees every key (prefill after L_k - L_q cached tokens); for
+ * L_q = L_k it is the usual lower triangle.  A row that sees no key (possible
+ * only when L_q > L_k) gets a zero row.  Arguments, layout, workspace and
+ * errors are those of attn_varlen_fwd; key tiles wholly above a row block's
+ * diagonal are skipped, and units are never split along keys.
+ */
+int attn_varlen_fwd_causal(const void* q, const void* k, const void* v,
+                           const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                           int num_seqs, int num_heads, int head_dim,
+                           void* out, cudaStream_t stream);
+
 /* Bytes of workspace attn_varlen_fwd_ws needs for num_seqs sequences
  * (0 for num_seqs < 0). */
 size_t attn_varlen_workspace_size(int num_seqs);

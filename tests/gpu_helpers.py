@@ -39,7 +39,7 @@ def device_inputs(x: dict, device):
 
 
 def run_cuda(vlp, x: dict, device="cuda", out_fill: int | None = None,
-             caller_workspace: bool = False):
+             caller_workspace: bool = False, causal: bool = False):
     """Run the CUDA path; returns the output as bf16 bits (uint16, [T, H, D]).
 
     ``out_fill``: int16 bit pattern to pre-fill the output with (default:
@@ -57,7 +57,7 @@ def run_cuda(vlp, x: dict, device="cuda", out_fill: int | None = None,
         out = vlp.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, out=out, workspace=ws)
         vlp.check(workspace=ws)
     else:
-        out = vlp.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, out=out)
+        out = vlp.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, out=out, causal=causal)
         vlp.check()
     return to_bits(out)
 
@@ -93,7 +93,7 @@ def abs_bits(bits: np.ndarray) -> np.ndarray:
     return bits & np.uint16(0x7FFF)
 
 
-def check_full(vlp, w, device="cuda", short_sequences=False, x=None):
+def check_full(vlp, w, device="cuda", short_sequences=False, x=None, causal=False):
     """Every output row of workload `w` (or of inputs `x`) against the oracle.
 
     ``short_sequences``: outputs are averages of a handful of values (very
@@ -101,8 +101,8 @@ def check_full(vlp, w, device="cuda", short_sequences=False, x=None):
     per-element bf16 bound applies above MAX_ABS (the mean bar still holds).
     """
     x = make_inputs(w) if x is None else x
-    got = run_cuda(vlp, x, device)
-    ref = oracle.attn_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"])
+    got = run_cuda(vlp, x, device, causal=causal)
+    ref = oracle.attn_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], causal=causal)
     cu = x["cu_q"]
     live = np.zeros(got.shape[0], bool)
     for i in range(len(cu) - 1):
@@ -110,18 +110,26 @@ def check_full(vlp, w, device="cuda", short_sequences=False, x=None):
             live[cu[i]:cu[i + 1]] = True
     bound = None
     if short_sequences:
-        absv = oracle.attn_varlen(x["q"], x["k"], abs_bits(x["v"]), x["cu_q"], x["cu_k"])
+        absv = oracle.attn_varlen(x["q"], x["k"], abs_bits(x["v"]), x["cu_q"], x["cu_k"],
+                                  causal=causal)
         bound = bf16_bound(ref[live], absv[live])
-    return assert_close(got[live], ref[live], w.name, bound=bound)
+    return assert_close(got[live], ref[live], w.name + (" causal" if causal else ""),
+                        bound=bound)
 
 
-def check_sampled(vlp, w, rows_per_head: int, device="cuda"):
+def check_sampled(vlp, w, rows_per_head: int, device="cuda", causal=False):
     """Seeded sample of output rows of workload `w` against the oracle."""
     x = make_inputs(w)
-    got = run_cuda(vlp, x, device)
+    got = run_cuda(vlp, x, device, causal=causal)
     rows = sample_rows(w, rows_per_head)
-    ref = oracle.attn_rows(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], rows)
-    return assert_close(got[rows[:, 0], rows[:, 1]], ref, w.name)
+    ref = oracle.attn_rows(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], rows, causal=causal)
+    bound = None
+    if causal:  # the first rows of a sequence average only a few values
+        absv = oracle.attn_rows(x["q"], x["k"], abs_bits(x["v"]), x["cu_q"], x["cu_k"], rows,
+                                causal=True)
+        bound = bf16_bound(ref, absv)
+    return assert_close(got[rows[:, 0], rows[:, 1]], ref,
+                        w.name + (" causal" if causal else ""), bound=bound)
 
 
 def check_rows(vlp, w, rows: np.ndarray, device="cuda", caller_workspace=False, x=None):

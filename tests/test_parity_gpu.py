@@ -255,3 +255,45 @@ def test_other_head_dims_sampled(cuda_lib, D):
     """A longer sequence at every extra head_dim: 512 rows per head."""
     w = Workload(f"L4500_H8_D{D}", (4500,), 8, D, seed=50 + D)
     check_sampled(cuda_lib, w, 512)
+
+
+# ------------------------------------------------------------------ causal
+CAUSAL = [
+    # (lens_q, lens_k or None, heads, head_dim): L_q = L_k across tile and
+    # unit boundaries, L_q < L_k (a cached prefix), L_q > L_k (leading rows
+    # that see no key), L_k = 0, every head_dim
+    ((1,), None, 2, 72), ((127,), None, 2, 72), ((129,), None, 2, 128), ((300,), None, 2, 72),
+    ((513,), None, 2, 128), ((700,), None, 3, 64), ((5, 130, 0, 257, 1, 64), None, 3, 72),
+    ((100, 7), (257, 1000), 2, 72), ((300,), (1000,), 2, 128), ((300,), (100,), 2, 72),
+    ((257,), (5,), 2, 128), ((400, 3), (0, 3), 2, 72), ((300,), None, 2, 96),
+    ((200, 31), (250, 600), 2, 80), ((640,), (113,), 1, 72), ((129,), (1,), 2, 64),
+]
+
+
+@pytest.mark.parametrize("lens_q,lens_k,H,D", CAUSAL)
+def test_causal_ragged_shapes(cuda_lib, lens_q, lens_k, H, D):
+    w = Workload(f"causal_{lens_q}_{lens_k}_{H}_{D}", lens_q, H, D,
+                 seed=300 + sum(lens_q) + D, seq_lens_k=lens_k)
+    check_full(cuda_lib, w, short_sequences=True, causal=True)
+
+
+@pytest.mark.parametrize("w", [C2, C3, C5], ids=lambda w: w.name)
+def test_causal_workloads_sampled(cuda_lib, w):
+    """The page's workloads under the causal mask: 256 seeded rows per head."""
+    check_sampled(cuda_lib, w, 256, causal=True)
+
+
+def test_causal_deterministic(cuda_lib):
+    x = make_inputs(C5)
+    a = run_cuda(cuda_lib, x, causal=True)
+    b = run_cuda(cuda_lib, x, causal=True)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_causal_last_row_equals_non_causal(cuda_lib):
+    """The bottom-right-aligned mask hides nothing from a sequence's last row."""
+    x = make_inputs(C1)
+    a = run_cuda(cuda_lib, x, causal=True)
+    b = run_cuda(cuda_lib, x)
+    last = int(x["cu_q"][-1]) - 1
+    np.testing.assert_array_equal(a[last], b[last])

@@ -37,6 +37,7 @@ SYMBOLS = {
     "attn_varlen_version": (_I, []),
     "attn_varlen_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "attn_varlen_last_cuda_error": (ctypes.c_char_p, []),
+    "attn_varlen_fwd_causal": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
 }
 
 _LOCK = threading.Lock()
@@ -106,7 +107,7 @@ def _check_inputs(q, k, v, cu_q, cu_k, out):
 
 
 def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, out=None, stream=None,
-                    workspace=None):
+                    workspace=None, causal=False):
     """softmax(q k^T / sqrt(head_dim)) v per packed sequence and head.
 
     q: bf16 [total_q, H, D]; k, v: bf16 [total_k, H, D]; cu_seqlens_q/k:
@@ -114,6 +115,8 @@ def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, out=None, stream=None,
     ``torch.empty_like(q)`` when not given; rows outside every query slice are
     left untouched).  ``workspace``: optional uint8 CUDA tensor of at least
     ``workspace_size(num_seqs)`` bytes, zero-filled before first use.
+    ``causal``: row r of a sequence sees keys j <= r + L_k - L_q
+    (attn_varlen_fwd_causal; library-owned workspace only).
     """
     import torch
     if out is None:
@@ -123,8 +126,14 @@ def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, out=None, stream=None,
     num_seqs = cu_seqlens_q.numel() - 1
     H, D = q.shape[1], q.shape[2]
     s = _stream_handle(stream, q.device)
+    if causal and workspace is not None:
+        raise ValueError("the causal entry point uses the library-owned workspace")
     with torch.cuda.device(q.device):
-        if workspace is None:
+        if causal:
+            rc = lib.attn_varlen_fwd_causal(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+                                            num_seqs, H, D, out.data_ptr(), s)
+        elif workspace is None:
             rc = lib.attn_varlen_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                      cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
                                      num_seqs, H, D, out.data_ptr(), s)

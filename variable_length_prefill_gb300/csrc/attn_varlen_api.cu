@@ -141,7 +141,7 @@ namespace {
 // items right after ws_layout(num_seqs).total.
 int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const int32_t* cu_k,
         int num_seqs, int num_heads, int head_dim, void* out, void* ws, int split_cap, int dev,
-        DeviceState& st, cudaStream_t stream) {
+        DeviceState& st, cudaStream_t stream, bool causal = false) {
   avp::PlanParams pp;
   std::memset(&pp, 0, sizeof(pp));
   const void* bases[avp::kMapsPerSeq] = {q, k, v};
@@ -157,6 +157,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const 
   pp.split_cap = split_cap;
   pp.grid = st.sm_count;
   pp.kv_rows = avp::kv_tile_rows(head_dim);
+  pp.causal = causal ? 1 : 0;
   pp.num_seqs = num_seqs;
   pp.num_heads = num_heads;
   pp.row_bytes = num_heads * head_dim * 2;
@@ -171,6 +172,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const 
   fp.out = static_cast<uint16_t*>(out);
   fp.num_seqs = num_seqs;
   fp.num_heads = num_heads;
+  fp.causal = causal ? 1 : 0;
   fp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
 
   const int slot = head_dim;
@@ -247,9 +249,9 @@ size_t attn_varlen_workspace_size(int num_seqs) {
   return avp::ws_layout(num_seqs).total;
 }
 
-int attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
-                    const int32_t* cu_seqlens_k, int num_seqs, int num_heads, int head_dim,
-                    void* out, cudaStream_t stream) {
+static int fwd_owned(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                     const int32_t* cu_seqlens_k, int num_seqs, int num_heads, int head_dim,
+                     void* out, cudaStream_t stream, bool causal) {
   int rc = check_args(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out);
   if (rc || num_seqs == 0) return rc;
   int dev = 0;
@@ -264,7 +266,21 @@ int attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* 
   if ((rc = ensure_workspace(st, avp::ws_layout(num_seqs).total + avp::split_layout(cap).total)))
     return rc;
   return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, st.ws, cap,
-             dev, st, stream);
+             dev, st, stream, causal);
+}
+
+int attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                    const int32_t* cu_seqlens_k, int num_seqs, int num_heads, int head_dim,
+                    void* out, cudaStream_t stream) {
+  return fwd_owned(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, stream,
+                   false);
+}
+
+int attn_varlen_fwd_causal(const void* q, const void* k, const void* v,
+                           const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int num_seqs,
+                           int num_heads, int head_dim, void* out, cudaStream_t stream) {
+  return fwd_owned(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, stream,
+                   true);
 }
 
 int attn_varlen_fwd_ws(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,

@@ -88,6 +88,7 @@ struct PlanParams {
   int split_cap;   // items the split region holds (0: no tail split)
   int grid;        // CTAs of the attention kernel
   int kv_rows;     // keys per K/V tile
+  int causal;      // causal mask: never split units along keys
   int num_seqs;
   int num_heads;
   int row_bytes;  // num_heads * head_dim * 2
@@ -117,6 +118,7 @@ struct FwdParams {
   uint16_t* out;
   int num_seqs;
   int num_heads;
+  int causal;        // 1: row r of a sequence sees keys <= r + L_k - L_q
   float scale_log2;  // head_dim^-1/2 * log2(e)
 };
 

@@ -206,7 +206,9 @@ struct Geometry {
 
 struct UnitInfo {
   int seq, head, q0, lq, lk, qbase;
-  int jb, nkv;     // this item's key tiles: [jb, jb + nkv)
+  int jb, nkv;     // this item's key tiles: [jb, jb + nkv) (Q tile 1, or 0 alone)
+  int nkv0;        // key tiles Q tile 0 needs (< nkv only with the causal mask)
+  int coff;        // causal mask: row r sees keys <= r + coff (coff = L_k - L_q)
   int chunks;      // items the unit is split into (1: not split)
   int part, part0, tail;  // split items: partial slot, the unit's first slot, tail unit
   bool t1;  // second Q tile holds at least one row
@@ -215,7 +217,8 @@ struct UnitInfo {
 __device__ __forceinline__ UnitInfo decode_unit(int u, const int32_t* __restrict__ order,
                                                 const int32_t* __restrict__ prefix, int num_seqs,
                                                 const int32_t* __restrict__ cu_q,
-                                                const int32_t* __restrict__ cu_k, int kn) {
+                                                const int32_t* __restrict__ cu_k, int kn,
+                                                bool causal) {
   // largest rank r in [0, num_seqs) with prefix[r] <= u
   int lo = 0, hi = num_seqs - 1;
   while (lo < hi) {
@@ -232,9 +235,22 @@ __device__ __forceinline__ UnitInfo decode_unit(int u, const int32_t* __restrict
   if (ui.lk < 0) ui.lk = 0;
   const int pairs = (ui.lq + kUnitRows - 1) / kUnitRows;
   ui.head = local / pairs;
-  ui.q0 = (local - ui.head * pairs) * kUnitRows;
+  const int qb = local - ui.head * pairs;
+  // causal: the last row blocks see the most keys, so they go first
+  ui.q0 = (causal ? pairs - 1 - qb : qb) * kUnitRows;
   ui.t1 = ui.q0 + kBlockM < ui.lq;
   ui.nkv = (ui.lk + kn - 1) / kn;
+  ui.nkv0 = ui.nkv;
+  ui.coff = ui.lk - ui.lq;
+  if (causal) {
+    // keys visible to the last row of each tile: min(L_k, row + 1 + coff)
+    const int last1 = min(ui.q0 + kUnitRows, ui.lq) - 1;
+    const int last0 = min(ui.q0 + kBlockM, ui.lq) - 1;
+    const int k1 = max(0, min(ui.lk, last1 + 1 + ui.coff));
+    const int k0 = max(0, min(ui.lk, last0 + 1 + ui.coff));
+    ui.nkv = (k1 + kn - 1) / kn;
+    ui.nkv0 = (k0 + kn - 1) / kn;
+  }
   ui.jb = 0;
   ui.chunks = 1;
   ui.part = ui.part0 = ui.tail = -1;
@@ -248,15 +264,17 @@ __device__ __forceinline__ UnitInfo decode_item(int it, const int32_t* __restric
                                                 const int32_t* __restrict__ cu_q,
                                                 const int32_t* __restrict__ cu_k, int kn,
                                                 int split_start, int num_units,
-                                                const int32_t* __restrict__ tail_prefix) {
-  if (it < split_start) return decode_unit(it, order, prefix, num_seqs, cu_q, cu_k, kn);
+                                                const int32_t* __restrict__ tail_prefix,
+                                                bool causal) {
+  if (it < split_start) return decode_unit(it, order, prefix, num_seqs, cu_q, cu_k, kn, causal);
   const int k = it - split_start;
   int lo = 0, hi = num_units - split_start - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (__ldg(tail_prefix + mid) <= k) lo = mid; else hi = mid - 1;
   }
-  UnitInfo ui = decode_unit(split_start + lo, order, prefix, num_seqs, cu_q, cu_k, kn);
+  // (split units are never causal: the plan does not split under the mask)
+  UnitInfo ui = decode_unit(split_start + lo, order, prefix, num_seqs, cu_q, cu_k, kn, causal);
   const int c0 = __ldg(tail_prefix + lo);
   const int chunks = __ldg(tail_prefix + lo + 1) - c0;
   if (chunks > 1) {
@@ -265,6 +283,7 @@ __device__ __forceinline__ UnitInfo decode_item(int it, const int32_t* __restric
     const int je = (int)(((long long)(c + 1) * ui.nkv) / chunks);
     ui.jb = jb;
     ui.nkv = je - jb;
+    ui.nkv0 = ui.nkv;
     ui.chunks = chunks;
     ui.part = k;
     ui.part0 = c0;
@@ -449,8 +468,8 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
   //    one warp searches T with shuffle reductions.
   const int U = s_carry;
   const int R = p.grid > 0 ? U % p.grid : 0;
-  const bool try_split = ATTN_VARLEN_TAIL_SPLIT && p.split_cap >= p.grid && p.grid > 0 &&
-                         R > 0 && R <= kLptMaxSeqs;
+  const bool try_split = ATTN_VARLEN_TAIL_SPLIT && !p.causal && p.split_cap >= p.grid &&
+                         p.grid > 0 && R > 0 && R <= kLptMaxSeqs;
   const int t0 = U - R;  // first tail unit
   if (try_split) {
     for (int r = tid; r < N; r += nt) {
@@ -709,7 +728,7 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       if (u >= num_items) break;
       if (leader) pending = atomicAdd(p.status + kHdrNextItem, 1);
       const UnitInfo ui = decode_item(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, G::KN,
-                                        split_start, num_units, tail_prefix);
+                                        split_start, num_units, tail_prefix, p.causal != 0);
       if (ui.nkv == 0) continue;
       const uint8_t* mq = p.ws + L.maps + (size_t)ui.seq * kMapsPerSeq * kMapBytes;
       const uint8_t* mk = mq + kMapBytes;
@@ -822,7 +841,7 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       const int u = next_item(k);
       if (u < 0 || u >= num_items) break;
       const UnitInfo ui = decode_item(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, G::KN,
-                                        split_start, num_units, tail_prefix);
+                                        split_start, num_units, tail_prefix, p.causal != 0);
       if (ui.nkv == 0) continue;
       if (!(ok = wait_(bar(G::B_Q_FULL), q_use & 1u))) break;
       ++q_use;
@@ -834,10 +853,14 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
         // it runs while that softmax is still in its exp2 phase.  A unit
         // without a second Q tile still has issuer 1 take part in the slot
         // releases, after each slot has filled, so no barrier runs ahead.
+        // Under the causal mask tile 0 may need fewer key tiles (nkv0) than
+        // the unit loads; its issuer then only takes part in the releases.
         const int t = mi;
         const bool has = t == 0 || ui.t1;
+        const int n_t = has ? (t == 0 ? ui.nkv0 : ui.nkv) : 0;
+        bool mine = false;  // this issuer has MMAs on the slot being released
         auto release = [&](uint32_t b) {
-          if (has)
+          if (mine)
             mma_commit_if(leader, b);
           else if (leader)
             mbar_arrive(b);
@@ -847,7 +870,8 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
           if (j < n) {
             const uint32_t itk = kv_item + (j == 0 ? 0u : 2u * j - 1u);
             if (!(ok = kv_full(itk))) break;
-            if (has) {
+            mine = j < n_t;
+            if (mine) {
               if (s_cnt[t] > 0 && !(ok = wait_(bar(G::B_S_FREE + t), (s_cnt[t] - 1) & 1u))) break;
               tc_fence_after();
               issue_s(t, stage_of(itk));
@@ -855,12 +879,14 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
               ++s_cnt[t];
             }
             release(bar(G::B_KV_EMPTY + stage_of(itk)));
+            mine = n_t > 0;  // commit after this issuer's last MMA on Q
             if (j == n - 1) release(bar(G::B_Q_EMPTY));
           }
           if (j >= 1) {
             const uint32_t itv = kv_item + (j == n ? 2u * n - 1u : 2u * j);
             if (!(ok = kv_full(itv))) break;
-            if (has) {
+            mine = j - 1 < n_t;
+            if (mine) {
               if (!(ok = wait_(bar(G::B_P_FULL + t), p_wait[t] & 1u))) break;
               ++p_wait[t];
               tc_fence_after();
@@ -877,11 +903,13 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
         {
           const uint32_t it = kv_item;
           if (!(ok = kv_full(it))) break;
-          ok = wait_pv_idle(0);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(0, stage_of(it));
-          mma_commit_if(leader, bar(G::B_S_FULL + 0));
+          if (ui.nkv0 > 0) {
+            ok = wait_pv_idle(0);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(0, stage_of(it));
+            mma_commit_if(leader, bar(G::B_S_FULL + 0));
+          }
           if (ui.t1) {
             ok = wait_pv_idle(1);
           if (!ok) break;
@@ -897,17 +925,21 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
           const uint32_t itk = itv + 1;
           const bool more = j + 1 < ui.nkv;
           if (!(ok = kv_full(itv))) break;
-          // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
-          if (!(ok = wait_(bar(G::B_P_FULL + 0), p_wait[0] & 1u))) break;
-          ++p_wait[0];
-          tc_fence_after();
-          issue_pv(0, stage_of(itv), j > 0);
-          mma_commit_if(leader, bar(G::B_PV_DONE + 0));
-          ++pv_cnt[0];
+          // tile 0 (for its nkv0 key tiles): O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
+          if (j < ui.nkv0) {
+            if (!(ok = wait_(bar(G::B_P_FULL + 0), p_wait[0] & 1u))) break;
+            ++p_wait[0];
+            tc_fence_after();
+            issue_pv(0, stage_of(itv), j > 0);
+            mma_commit_if(leader, bar(G::B_PV_DONE + 0));
+            ++pv_cnt[0];
+          }
           if (more) {
             if (!(ok = kv_full(itk))) break;
+          }
+          if (more && j + 1 < ui.nkv0) {
             ok = wait_pv_idle(0);
-          if (!ok) break;
+            if (!ok) break;
             tc_fence_after();
             issue_s(0, stage_of(itk));
             mma_commit_if(leader, bar(G::B_S_FULL + 0));
@@ -964,12 +996,16 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       const int u = next_item(k);
       if (u < 0 || u >= num_items) break;
       const UnitInfo ui = decode_item(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, KN,
-                                        split_start, num_units, tail_prefix);
+                                        split_start, num_units, tail_prefix, p.causal != 0);
       if (t == 1 && !ui.t1) continue;
       const int row = ui.q0 + kBlockM * t + r;
       const bool valid = row < ui.lq;
       uint16_t* orow = p.out + ((size_t)(ui.qbase + row) * p.num_heads + ui.head) * D;
-      if (ui.nkv == 0) {
+      const int nsteps = t == 0 ? ui.nkv0 : ui.nkv;  // key tiles of this Q tile
+      // keys this row may see: all L_k, or under the causal mask
+      // min(L_k, row + 1 + L_k - L_q) (<= 0: none, the row is zero)
+      const int klim = p.causal ? min(ui.lk, row + 1 + ui.coff) : ui.lk;
+      if (nsteps == 0) {
         if (valid) {
           uint4* o4 = reinterpret_cast<uint4*>(orow);
 #pragma unroll
@@ -978,14 +1014,17 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
         continue;
       }
       float m = 0.f, l = 0.f;
-      for (int j = 0; j < ui.nkv; ++j) {
+      for (int j = 0; j < nsteps; ++j) {
         if (!(ok = wait_(bar(G::B_S_FULL + t), s_wait & 1u))) break;
         ++s_wait;
         tc_fence_after();
         uint32_t s[KN];
-        // keys past the end of the sequence in its last tile
-        const int lim = ui.lk - (ui.jb + j) * KN;
-        const bool tail = lim < KN;  // only the last key tile can be partial
+        // keys past the end of the sequence (or past this row's causal
+        // limit) in this tile are masked
+        const int lim = klim - (ui.jb + j) * KN;
+        // warp-uniform: both branches below hold tcgen05.wait::ld, which the
+        // whole warp must execute together; masking at lim >= KN is a no-op
+        const bool tail = __any_sync(0xffffffffu, lim < KN);
         tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
         tmem_wait_ld();
@@ -1038,7 +1077,8 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
         }
         const float mxs = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
         if (j == 0) {
-          m = mxs;
+          // a row that sees no key keeps m = 0: all its weights are 0
+          m = mxs == -INFINITY ? 0.f : mxs;
         } else {
           const bool need = mxs > m + kRescaleThreshold;
           if (__any_sync(0xffffffffu, need)) {
@@ -1119,7 +1159,7 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
                           r, m, l, orow, valid, ui.part, ui.part0, ui.tail, ui.chunks);
         continue;
       }
-      const float inv = 1.0f / l;
+      const float inv = l > 0.f ? 1.0f / l : 0.f;
 #pragma unroll
       for (int c = 0; c < G::DP; c += 16) {
         uint32_t o[16];
