@@ -21,6 +21,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "paged_oracle.c")]
 _BUILD = os.path.join(_HERE, "_build")
 _LOCK = threading.Lock()
 _LIBS: dict = {}
@@ -37,10 +38,10 @@ def build(mutation: int = 0, out_dir: str | None = None) -> str:
     name = "liboracle.so" if mutation == 0 else f"liboracle_mut{mutation}.so"
     path = os.path.join(out_dir, name)
     if (not os.path.exists(path)
-            or os.path.getmtime(path) < os.path.getmtime(_SRC)):
+            or os.path.getmtime(path) < max(os.path.getmtime(f) for f in _SRCS)):
         tmp = path + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
-               "-o", tmp, _SRC, "-lm"]
+               "-o", tmp, *_SRCS, "-lm"]
         if mutation:
             cmd.insert(1, f"-DORACLE_MUTATION={int(mutation)}")
         subprocess.run(cmd, check=True)
@@ -61,6 +62,8 @@ def _lib(mutation: int = 0):
             lib.oracle_attn_rows.restype = i
             lib.oracle_max_threads.argtypes = [i]
             lib.oracle_max_threads.restype = i
+            lib.oracle_paged_decode.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, p]
+            lib.oracle_paged_decode.restype = i
             _LIBS[mutation] = lib
         return _LIBS[mutation]
 
@@ -118,4 +121,32 @@ def attn_rows(q, k, v, cu_q, cu_k, rows, nthreads: int = 0,
         rows.shape[0], out.ctypes.data, int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_attn_rows failed with {rc}")
+    return out
+
+
+def paged_decode(query, k_cache, v_cache, block_tables, seq_lens, dtype: str = "bf16",
+                 mutation: int = 0) -> np.ndarray:
+    """Paged single-query decode, float64 [num_seqs, Hq, D].
+
+    ``query`` [num_seqs, Hq, D], ``k_cache`` [num_blocks, Hkv, D / 8,
+    block_size, 8], ``v_cache`` [num_blocks, Hkv, D, block_size]: bit patterns
+    (uint16) of ``dtype`` ("bf16" or "fp16"); ``block_tables`` int32
+    [num_seqs, max_blocks]; ``seq_lens`` int32 [num_seqs].
+    """
+    query = np.ascontiguousarray(query, dtype=np.uint16)
+    k_cache = np.ascontiguousarray(k_cache, dtype=np.uint16)
+    v_cache = np.ascontiguousarray(v_cache, dtype=np.uint16)
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    n, hq, d = query.shape
+    hkv, bs = v_cache.shape[1], v_cache.shape[3]
+    if k_cache.shape != (v_cache.shape[0], hkv, d // 8, bs, 8) or v_cache.shape[2] != d:
+        raise ValueError("cache shapes do not match the query")
+    out = np.zeros((n, hq, d), dtype=np.float64)
+    rc = _lib(mutation).oracle_paged_decode(
+        query.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data, tables.ctypes.data,
+        lens.ctypes.data, n, hq, hkv, d, bs, tables.shape[1] if tables.ndim == 2 else 0,
+        1 if dtype == "fp16" else 0, out.ctypes.data)
+    if rc != 0:
+        raise RuntimeError(f"oracle_paged_decode failed with {rc}")
     return out
