@@ -53,6 +53,7 @@ extern "C" {
 #define ATTN_VARLEN_ERR_WORKSPACE_SMALL   -8  /* caller workspace below the minimum */
 #define ATTN_VARLEN_ERR_DRIVER            -9  /* tensor-map encoder unavailable     */
 #define ATTN_VARLEN_ERR_NOALLOC_LIMIT    -10  /* num_seqs above the fixed scratch   */
+#define ATTN_VARLEN_ERR_BAD_BLOCK_TABLE  -11  /* paged decode: block id out of range */
 
 /*
  * attn_varlen_fwd -- the attention forward described above.

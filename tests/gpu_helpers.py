@@ -74,8 +74,14 @@ def bf16_bound(ref: np.ndarray, ref_absv: np.ndarray) -> np.ndarray:
 
 
 def assert_close(got_bits, ref, what="", bound=None):
-    """The stated bar; with ``bound``, elements above MAX_ABS must stay inside it."""
-    err = np.abs(bf16_bits_to_f64(got_bits) - ref)
+    """The stated bar; with ``bound``, elements above MAX_ABS must stay inside it.
+    ``got_bits``: bf16 bit patterns."""
+    return assert_close_values(bf16_bits_to_f64(got_bits), ref, what, bound)
+
+
+def assert_close_values(got, ref, what="", bound=None):
+    """assert_close for outputs already widened to float64."""
+    err = np.abs(np.asarray(got, dtype=np.float64) - ref)
     mx, mean = float(err.max()) if err.size else 0.0, float(err.mean()) if err.size else 0.0
     REPORT.append((what, err.size, mx, mean))
     assert mean <= MEAN_ABS, f"{what}: mean|err| {mean:.3e} > {MEAN_ABS}"

@@ -10,14 +10,17 @@ import pytest
 import variable_length_prefill_gb300 as vlp
 from variable_length_prefill_gb300 import _binding as B
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
-                      "include", "attn_varlen.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADER = os.path.join(INCLUDE, "attn_varlen.h")
 
 
 def _declared():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return set(re.findall(r"\b(attn_varlen_\w+)\s*\(", src))
+    names = set()
+    for f in sorted(os.listdir(INCLUDE)):
+        if f.endswith(".h"):
+            src = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, f)).read(), flags=re.S)
+            names |= set(re.findall(r"\b((?:attn_varlen|paged_attn)_\w+)\s*\(", src))
+    return names
 
 
 def _codes():
@@ -38,7 +41,8 @@ def test_return_codes_match_header():
     codes = _codes()
     assert codes["OK"] == B.OK
     for name in ("INVALID_ARG", "UNSUPPORTED_DIM", "MISALIGNED", "UNSUPPORTED_DEVICE",
-                 "CUDA", "OOM", "DEVICE_TIMEOUT", "WORKSPACE_SMALL", "DRIVER", "NOALLOC_LIMIT"):
+                 "CUDA", "OOM", "DEVICE_TIMEOUT", "WORKSPACE_SMALL", "DRIVER", "NOALLOC_LIMIT",
+                 "BAD_BLOCK_TABLE"):
         assert codes["ERR_" + name] == getattr(B, "ERR_" + name)
     for name, c in codes.items():
         if name == "NOALLOC_MAX_SEQS":
@@ -103,3 +107,20 @@ def test_product_path_has_no_oracle_dependency():
                 text = open(os.path.join(root, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "attn_oracle" not in text, f
+
+
+@pytest.mark.parametrize("args,code", [
+    # (query, k, v, tables, lens, n, Hq, Hkv, D, bs, max_blocks, num_blocks, dtype, out)
+    ((P, P, P, P, P, -1, 4, 4, 128, 16, 1, 1, 0, P, None), B.ERR_INVALID_ARG),
+    ((P, P, P, P, P, 1, 6, 4, 128, 16, 1, 1, 0, P, None), B.ERR_INVALID_ARG),   # Hq % Hkv
+    ((P, P, P, P, P, 1, 4, 4, 96, 16, 1, 1, 0, P, None), B.ERR_UNSUPPORTED_DIM),
+    ((P, P, P, P, P, 1, 4, 4, 128, 32, 1, 1, 0, P, None), B.ERR_INVALID_ARG),   # block_size
+    ((P, P, P, P, P, 1, 4, 4, 128, 16, 1, 1, 2, P, None), B.ERR_INVALID_ARG),   # dtype
+    ((P, P, P, P, P, 1, 4, 4, 128, 16, 0, 1, 0, P, None), B.ERR_INVALID_ARG),   # max_blocks
+    ((None, P, P, P, P, 1, 4, 4, 128, 16, 1, 1, 0, P, None), B.ERR_INVALID_ARG),
+    ((P + 8, P, P, P, P, 1, 4, 4, 128, 16, 1, 1, 0, P, None), B.ERR_MISALIGNED),
+    ((P, P, P, P + 2, P, 1, 4, 4, 128, 16, 1, 1, 0, P, None), B.ERR_MISALIGNED),
+    ((None, None, None, None, None, 0, 4, 4, 128, 16, 0, 0, 0, None, None), B.OK),
+])
+def test_paged_argument_checks_need_no_gpu(args, code):
+    assert vlp.load().paged_attn_decode(*args) == code

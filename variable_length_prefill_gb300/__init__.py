@@ -2,14 +2,15 @@
 
 The computation is atrex-bench "attention_forward" (page #001, reference.py,
 Model.forward): per packed sequence and head, softmax(Q K^T / sqrt(D)) V,
-non-causal, bf16 in and out.  It runs in a hand-written sm_103a CUDA library
-(TMA, tcgen05 MMA into TMEM, warp-specialised online softmax) behind the C
-ABI in include/attn_varlen.h; this package is a thin ctypes binding.
+non-causal (or, as an option, causal), bf16 in and out.  It runs in a
+hand-written sm_103a CUDA library (TMA, tcgen05 MMA into TMEM,
+warp-specialised online softmax) behind the C ABI in include/attn_varlen.h;
+the same library holds the paged single-query decode of
+include/paged_attn_decode.h.  This package is a thin ctypes binding.
 """
 from ._binding import (AttnVarlenError, SYMBOLS, attn_varlen_fwd, attn_varlen_fwd_noalloc,
-                       check, load, strerror, workspace_size)
+                       check, load, paged_attn_decode, strerror, workspace_size)
 from .build import build, lib_path
 
 __all__ = ["AttnVarlenError", "SYMBOLS", "attn_varlen_fwd", "attn_varlen_fwd_noalloc", "build",
-           "check",
-           "lib_path", "load", "strerror", "workspace_size"]
+           "check", "lib_path", "load", "paged_attn_decode", "strerror", "workspace_size"]

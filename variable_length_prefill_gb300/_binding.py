@@ -23,6 +23,7 @@ ERR_DEVICE_TIMEOUT = -7
 ERR_WORKSPACE_SMALL = -8
 ERR_DRIVER = -9
 ERR_NOALLOC_LIMIT = -10
+ERR_BAD_BLOCK_TABLE = -11
 NOALLOC_MAX_SEQS = 1024
 
 # Every symbol the header declares, with (restype, argtypes).
@@ -38,6 +39,7 @@ SYMBOLS = {
     "attn_varlen_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "attn_varlen_last_cuda_error": (ctypes.c_char_p, []),
     "attn_varlen_fwd_causal": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "paged_attn_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
 }
 
 _LOCK = threading.Lock()
@@ -180,4 +182,40 @@ def attn_varlen_fwd_noalloc(q, k, v, cu_seqlens_q, cu_seqlens_k, out, stream=Non
                                             num_seqs, q.shape[1], q.shape[2], out.data_ptr(), s)
     if rc != OK:
         raise AttnVarlenError(rc, "attn_varlen_fwd_noalloc")
+    return out
+
+
+def paged_attn_decode(query, k_cache, v_cache, block_tables, seq_lens, out=None, stream=None):
+    """One decode step over a paged KV cache (include/paged_attn_decode.h).
+
+    query [num_seqs, Hq, D]; k_cache [num_blocks, Hkv, D/8, 16, 8]; v_cache
+    [num_blocks, Hkv, D, 16], all bf16 or all fp16 CUDA tensors;
+    block_tables int32 [num_seqs, max_blocks]; seq_lens int32 [num_seqs].
+    Returns ``out`` (allocated like ``query`` when not given).
+    """
+    import torch
+    if out is None:
+        out = torch.empty_like(query)
+    if query.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("query must be bf16 or fp16")
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("out", out)):
+        if t.dtype != query.dtype or not t.is_contiguous() or t.device != query.device:
+            raise ValueError(f"{name} must be a contiguous {query.dtype} tensor on {query.device}")
+    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens)):
+        if t.dtype != torch.int32 or not t.is_contiguous() or t.device != query.device:
+            raise ValueError(f"{name} must be a contiguous int32 tensor on {query.device}")
+    if query.dim() != 3 or k_cache.dim() != 5 or v_cache.dim() != 4 or block_tables.dim() != 2:
+        raise ValueError("query [S, Hq, D], k_cache [B, Hkv, D/8, bs, 8], v_cache [B, Hkv, D, bs], "
+                         "block_tables [S, max_blocks]")
+    num_seqs, hq, d = query.shape
+    num_blocks, hkv, _, bs = v_cache.shape
+    lib = load()
+    s = _stream_handle(stream, query.device)
+    with torch.cuda.device(query.device):
+        rc = lib.paged_attn_decode(query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                   block_tables.data_ptr(), seq_lens.data_ptr(), num_seqs, hq,
+                                   hkv, d, bs, block_tables.shape[1], num_blocks,
+                                   1 if query.dtype == torch.float16 else 0, out.data_ptr(), s)
+    if rc != OK:
+        raise AttnVarlenError(rc, "paged_attn_decode")
     return out

@@ -13,6 +13,8 @@
 
 #include "attn_varlen.h"
 #include "attn_varlen_internal.h"
+#include "paged_attn_decode.h"
+#include "paged_decode_internal.h"
 
 namespace {
 
@@ -235,6 +237,7 @@ int read_and_clear_status(void* ws, cudaStream_t stream) {
     const int zero = 0;
     e = cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return fail_cuda(e);
+    if (status == avp::kPagedStatusBadBlock) return ATTN_VARLEN_ERR_BAD_BLOCK_TABLE;
     return ATTN_VARLEN_ERR_DEVICE_TIMEOUT;
   }
   return ATTN_VARLEN_OK;
@@ -331,6 +334,52 @@ int attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v,
              st, stream);
 }
 
+int paged_attn_decode(const void* query, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                      int num_query_heads, int num_kv_heads, int head_size, int block_size,
+                      int max_blocks_per_seq, int num_blocks, int dtype, void* out,
+                      cudaStream_t stream) {
+  if (num_seqs < 0 || num_query_heads < 1 || num_kv_heads < 1 ||
+      num_query_heads % num_kv_heads != 0)
+    return ATTN_VARLEN_ERR_INVALID_ARG;
+  if (dtype != PAGED_ATTN_BF16 && dtype != PAGED_ATTN_FP16) return ATTN_VARLEN_ERR_INVALID_ARG;
+  if (!avp::paged_head_size_supported(head_size)) return ATTN_VARLEN_ERR_UNSUPPORTED_DIM;
+  if (block_size != 16) return ATTN_VARLEN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return ATTN_VARLEN_OK;
+  if (max_blocks_per_seq < 1 || num_blocks < 1) return ATTN_VARLEN_ERR_INVALID_ARG;
+  if (!query || !k_cache || !v_cache || !block_tables || !seq_lens || !out)
+    return ATTN_VARLEN_ERR_INVALID_ARG;
+  auto a16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+  auto a4 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; };
+  if (!a16(query) || !a16(k_cache) || !a16(v_cache) || !a16(out) || !a4(block_tables) ||
+      !a4(seq_lens))
+    return ATTN_VARLEN_ERR_MISALIGNED;
+  int dev = 0;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if ((rc = probe_device(dev, st))) return rc;
+  if ((rc = ensure_workspace(st, 256))) return rc;  // the status word
+  avp::PagedParams p;
+  p.query = query;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.status = static_cast<int*>(st.ws);
+  p.num_seqs = num_seqs;
+  p.num_query_heads = num_query_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.qpk = num_query_heads / num_kv_heads;
+  p.head_size = head_size;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_size));
+  return map_cuda(avp::launch_paged_decode(p, dtype == PAGED_ATTN_FP16, stream));
+}
+
 int attn_varlen_check(cudaStream_t stream) {
   int dev = 0;
   int rc = current_device(&dev);
@@ -361,6 +410,8 @@ const char* attn_varlen_strerror(int code) {
     case ATTN_VARLEN_ERR_DEVICE_TIMEOUT: return "a kernel wait ran out of time";
     case ATTN_VARLEN_ERR_WORKSPACE_SMALL: return "workspace smaller than attn_varlen_workspace_size()";
     case ATTN_VARLEN_ERR_DRIVER: return "cuTensorMapEncodeTiled unavailable or failed";
+    case ATTN_VARLEN_ERR_BAD_BLOCK_TABLE:
+      return "paged decode: a block table entry was outside [0, num_blocks)";
     case ATTN_VARLEN_ERR_NOALLOC_LIMIT:
       return "num_seqs exceeds ATTN_VARLEN_NOALLOC_MAX_SEQS (1024), the fixed scratch of "
              "attn_varlen_fwd_noalloc";
