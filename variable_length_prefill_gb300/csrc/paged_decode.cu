@@ -13,7 +13,9 @@
 // (block, KV head) holds 4 KB of contiguous K (D = 128) and 4 KB of V, so the
 // kernel is bound by HBM (or, for the page's small shapes, by latency).  It
 // uses plain coalesced 16-byte loads, no tensor cores:
-//   CTA  = (sequence, KV head, group of up to kMaxQ query heads), 4 warps;
+//   CTA  = (sequence, KV head, group of up to MQ query heads), 4 warps, MQ
+//          the power of two (at most 8) that covers the query heads per KV
+//          head, so registers scale with the group;
 //   warp = every 4th block of the context, an exp2 online softmax per head;
 //   keys:   lane = (token 0-15, half of the head dimension): 16-byte chunks
 //           [c][token][8] of one half are 256 contiguous bytes per warp load,
@@ -21,6 +23,9 @@
 //   values: lane = D/32 consecutive dimensions, each a 32-byte row of the
 //           block's 16 tokens;
 //   the four warps' (m, l, O) merge through shared memory at the end.
+// A block's value rows are loaded together with its key chunks, and each
+// warp reads its next block-table entry before working on the current block,
+// so a block costs one dependent memory round trip.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -34,7 +39,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kBlock = 16;   // tokens per cache block
-constexpr int kMaxQ = 8;     // query heads per CTA
+constexpr int kMaxQ = 8;     // query heads per CTA at most
 
 template <typename T>
 __device__ __forceinline__ float to_f32(T x);
@@ -64,22 +69,25 @@ __device__ __forceinline__ float fast_ex2(float x) {
   return y;
 }
 
-template <int D, typename T>
+template <int D, typename T, int MQ>
 __global__ void __launch_bounds__(32 * kWarps) paged_decode_kernel(const __grid_constant__ PagedParams p) {
   constexpr int NCH = D / 8;        // 16-byte chunks of a key row
   constexpr int HCH = NCH / 2;      // chunks per lane (one half of the row)
   constexpr int DPL = D / 32;       // value dimensions per lane
-  __shared__ float s_q[kMaxQ][D];                  // scaled queries
-  __shared__ float s_p[kWarps][kMaxQ][kBlock];     // one block's weights per warp
-  __shared__ float s_m[kWarps][kMaxQ], s_l[kWarps][kMaxQ];
-  __shared__ float s_o[kWarps][kMaxQ][D];
+  // query row: the second half of the dimensions sits 4 floats further on, so
+  // the two half-warps' broadcast reads fall in different banks
+  constexpr int QROW = D + 4;
+  __shared__ __align__(16) float s_q[MQ][QROW];   // scaled queries
+  __shared__ float s_p[kWarps][MQ][kBlock];       // one block's weights per warp
+  __shared__ float s_m[kWarps][MQ], s_l[kWarps][MQ];
+  __shared__ float s_o[kWarps][MQ][D];
 
-  const int ngroups = (p.qpk + kMaxQ - 1) / kMaxQ;
+  const int ngroups = (p.qpk + MQ - 1) / MQ;
   const int seq = blockIdx.x / (p.num_kv_heads * ngroups);
   const int rem = blockIdx.x - seq * p.num_kv_heads * ngroups;
   const int g = rem / ngroups;
-  const int h0 = g * p.qpk + (rem - g * ngroups) * kMaxQ;   // first query head of the CTA
-  const int nq = min(kMaxQ, g * p.qpk + p.qpk - h0);
+  const int h0 = g * p.qpk + (rem - g * ngroups) * MQ;   // first query head of the CTA
+  const int nq = min(MQ, g * p.qpk + p.qpk - h0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const T* q = static_cast<const T*>(p.query) + ((size_t)seq * p.num_query_heads + h0) * D;
   T* out = static_cast<T*>(p.out) + ((size_t)seq * p.num_query_heads + h0) * D;
@@ -90,16 +98,16 @@ __global__ void __launch_bounds__(32 * kWarps) paged_decode_kernel(const __grid_
     for (int i = threadIdx.x; i < nq * D; i += blockDim.x) out[i] = from_f32<T>(0.f);
     return;
   }
-  for (int i = threadIdx.x; i < kMaxQ * D; i += blockDim.x) {
-    const int hh = i / D;
-    s_q[hh][i % D] = hh < nq ? to_f32<T>(q[i]) * p.scale_log2 : 0.f;
+  for (int i = threadIdx.x; i < MQ * D; i += blockDim.x) {
+    const int hh = i / D, d = i % D;
+    s_q[hh][d + (d >= D / 2 ? 4 : 0)] = hh < nq ? to_f32<T>(q[i]) * p.scale_log2 : 0.f;
   }
   __syncthreads();
 
   const int tok = lane & 15, half = lane >> 4;
-  float m[kMaxQ], l[kMaxQ], o[kMaxQ][DPL];
+  float m[MQ], l[MQ], o[MQ][DPL];
 #pragma unroll
-  for (int hh = 0; hh < kMaxQ; ++hh) {
+  for (int hh = 0; hh < MQ; ++hh) {
     m[hh] = -INFINITY;
     l[hh] = 0.f;
 #pragma unroll
@@ -107,8 +115,10 @@ __global__ void __launch_bounds__(32 * kWarps) paged_decode_kernel(const __grid_
   }
   const int nblk = (L + kBlock - 1) / kBlock;
   const int32_t* table = p.block_tables + (size_t)seq * p.max_blocks;
+  int b_next = warp < nblk ? __ldg(table + warp) : 0;
   for (int jb = warp; jb < nblk; jb += kWarps) {
-    const int b = table[jb];
+    const int b = b_next;
+    if (jb + kWarps < nblk) b_next = __ldg(table + jb + kWarps);  // next block's id, early
     if (b < 0 || b >= p.num_blocks) {  // never dereference a bad block id
       if (lane == 0) atomicOr(p.status, kPagedStatusBadBlock);
       continue;
@@ -116,19 +126,27 @@ __global__ void __launch_bounds__(32 * kWarps) paged_decode_kernel(const __grid_
     // scores of this lane's token for every query head (half the dimensions)
     const uint4* kb = reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_cache) +
                                                      ((size_t)b * p.num_kv_heads + g) * D * kBlock);
-    float acc[kMaxQ];
+    float acc[MQ];
 #pragma unroll
-    for (int hh = 0; hh < kMaxQ; ++hh) acc[hh] = 0.f;
+    for (int hh = 0; hh < MQ; ++hh) acc[hh] = 0.f;
     uint4 kc[HCH];
 #pragma unroll
     for (int c = 0; c < HCH; ++c) kc[c] = __ldg(kb + (half * HCH + c) * kBlock + tok);
+    const T* vb = static_cast<const T*>(p.v_cache) + ((size_t)b * p.num_kv_heads + g) * D * kBlock +
+                  (size_t)lane * DPL * kBlock;
+    uint4 vc[2 * DPL];  // this lane's value rows, in flight with the keys
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) {
+      vc[2 * e] = __ldg(reinterpret_cast<const uint4*>(vb + e * kBlock));
+      vc[2 * e + 1] = __ldg(reinterpret_cast<const uint4*>(vb + e * kBlock) + 1);
+    }
 #pragma unroll
     for (int c = 0; c < HCH; ++c) {
       float kf[8];
       unpack8<T>(kc[c], kf);
-      const int d0 = (half * HCH + c) * 8;
+      const int d0 = (half * HCH + c) * 8 + half * 4;  // padded query row
 #pragma unroll
-      for (int hh = 0; hh < kMaxQ; ++hh) {
+      for (int hh = 0; hh < MQ; ++hh) {
         if (hh < nq) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) acc[hh] = fmaf(s_q[hh][d0 + e], kf[e], acc[hh]);
@@ -137,7 +155,7 @@ __global__ void __launch_bounds__(32 * kWarps) paged_decode_kernel(const __grid_
     }
     const bool live = jb * kBlock + tok < L;
 #pragma unroll
-    for (int hh = 0; hh < kMaxQ; ++hh) {
+    for (int hh = 0; hh < MQ; ++hh) {
       if (hh >= nq) continue;
       float sc = acc[hh] + __shfl_xor_sync(0xffffffffu, acc[hh], 16);
       sc = live ? sc : -INFINITY;
@@ -158,16 +176,13 @@ __global__ void __launch_bounds__(32 * kWarps) paged_decode_kernel(const __grid_
     }
     __syncwarp();
     // values: this lane's DPL dimensions, 16 tokens each
-    const T* vb = static_cast<const T*>(p.v_cache) + ((size_t)b * p.num_kv_heads + g) * D * kBlock +
-                  (size_t)lane * DPL * kBlock;
 #pragma unroll
     for (int e = 0; e < DPL; ++e) {
-      const uint4* row = reinterpret_cast<const uint4*>(vb + e * kBlock);
       float v0[8], v1[8];
-      unpack8<T>(__ldg(row), v0);
-      unpack8<T>(__ldg(row + 1), v1);
+      unpack8<T>(vc[2 * e], v0);
+      unpack8<T>(vc[2 * e + 1], v1);
 #pragma unroll
-      for (int hh = 0; hh < kMaxQ; ++hh) {
+      for (int hh = 0; hh < MQ; ++hh) {
         if (hh >= nq) continue;
         float a = o[hh][e];
 #pragma unroll
@@ -183,13 +198,13 @@ __global__ void __launch_bounds__(32 * kWarps) paged_decode_kernel(const __grid_
   // merge the warps: O = sum_w 2^(m_w - m*) O_w, l likewise
   if (lane == 0) {
 #pragma unroll
-    for (int hh = 0; hh < kMaxQ; ++hh) {
+    for (int hh = 0; hh < MQ; ++hh) {
       s_m[warp][hh] = m[hh];
       s_l[warp][hh] = l[hh];
     }
   }
 #pragma unroll
-  for (int hh = 0; hh < kMaxQ; ++hh)
+  for (int hh = 0; hh < MQ; ++hh)
 #pragma unroll
     for (int e = 0; e < DPL; ++e) s_o[warp][hh][lane * DPL + e] = o[hh][e];
   __syncthreads();
@@ -210,14 +225,24 @@ __global__ void __launch_bounds__(32 * kWarps) paged_decode_kernel(const __grid_
   }
 }
 
-template <int D, typename T>
-cudaError_t launch_t(const PagedParams& p, cudaStream_t stream) {
-  const int ngroups = (p.qpk + kMaxQ - 1) / kMaxQ;
+template <int D, typename T, int MQ>
+cudaError_t launch_mq(const PagedParams& p, cudaStream_t stream) {
+  const int ngroups = (p.qpk + MQ - 1) / MQ;
   const long long grid = (long long)p.num_seqs * p.num_kv_heads * ngroups;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  paged_decode_kernel<D, T><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
+  paged_decode_kernel<D, T, MQ><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+// The head group is the smallest power of two (at most kMaxQ) covering the
+// query heads of one KV head.
+template <int D, typename T>
+cudaError_t launch_t(const PagedParams& p, cudaStream_t stream) {
+  if (p.qpk <= 1) return launch_mq<D, T, 1>(p, stream);
+  if (p.qpk <= 2) return launch_mq<D, T, 2>(p, stream);
+  if (p.qpk <= 4) return launch_mq<D, T, 4>(p, stream);
+  return launch_mq<D, T, kMaxQ>(p, stream);
 }
 
 }  // namespace
