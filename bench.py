@@ -30,7 +30,8 @@ if ROOT not in sys.path:
 
 import numpy as np  # noqa: E402
 
-from workloads import C1, C2, C3, C4, C5, CONFIGS, make_inputs, sample_rows  # noqa: E402
+from workloads import (C1, C2, C3, C4, C5, CONFIGS, PAGED_CONFIGS, make_inputs,  # noqa: E402
+                       make_paged_inputs, sample_rows)
 
 HEADLINE = C2
 METRIC = "varlen attn fwd TFLOP/s (4*sum(L^2)*H*D)"
@@ -345,6 +346,41 @@ def run_ours(args, rank, world, local_rank):
                 entry["us_per_call_in_graph"] = round(graph_us_per_call(fn, stream), 2)
             shapes[ws.name] = entry
             del ts, os_
+        vlp.check()
+        # the causal variant of the same workloads (FLOPs of the visible pairs)
+        for ws in (C2, C3, C5):
+            xs, ts, cq, ck = device_inputs(ws)
+            os_ = torch.empty_like(ts["q"])
+            fn = lambda: vlp.attn_varlen_fwd(ts["q"], ts["k"], ts["v"], cq, ck, out=os_,  # noqa: E731
+                                             causal=True)
+            for _ in range(3):
+                fn()
+            us = statistics.median(time_calls(fn, 10, flush, stream)) * 1e3
+            vis = sum(int(np.clip(np.arange(a) + 1 + b - a, 0, b).sum())
+                      for a, b in zip(ws.seq_lens_q, ws.lens_k) if a > 0 and b > 0)
+            shapes[ws.name + "_causal"] = {
+                "us": round(us, 2), "tflops": round(4.0 * vis * ws.num_heads * ws.head_dim /
+                                                    (us * 1e-6) / 1e12, 2)}
+            del ts, os_
+        # paged single-query decode: the page's shape table, HBM-bound
+        for name, pw in PAGED_CONFIGS.items():
+            xs = make_paged_inputs(pw)
+            tdt = torch.bfloat16 if pw.dtype == "bf16" else torch.float16
+            pt = {n: torch.from_numpy(xs[n].view(np.int16)).view(tdt).to(dev)
+                  for n in ("query", "k_cache", "v_cache")}
+            tb = torch.from_numpy(xs["block_tables"]).to(dev)
+            ln = torch.from_numpy(xs["seq_lens"]).to(dev)
+            po = torch.empty_like(pt["query"])
+            fn = lambda: vlp.paged_attn_decode(pt["query"], pt["k_cache"], pt["v_cache"],  # noqa: E731
+                                               tb, ln, out=po)
+            for _ in range(3):
+                fn()
+            us = statistics.median(time_calls(fn, 20, flush, stream)) * 1e3
+            shapes["paged_" + pw.name] = {
+                "us": round(us, 2),
+                "gbs_algorithmic": round(pw.algorithmic_bytes() / (us * 1e-6) / 1e9, 1),
+                "pct_hbm": round(100.0 * pw.algorithmic_bytes() / (us * 1e-6) / 1e9 /
+                                 peaks["hbm_gbs"], 2)}
         vlp.check()
 
     if rank != 0:
