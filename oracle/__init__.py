@@ -21,7 +21,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
-_SRCS = [_SRC, os.path.join(_HERE, "paged_oracle.c")]
+_SRCS = [_SRC, os.path.join(_HERE, "paged_oracle.c"), os.path.join(_HERE, "chunk_o_oracle.c")]
 _BUILD = os.path.join(_HERE, "_build")
 _LOCK = threading.Lock()
 _LIBS: dict = {}
@@ -64,6 +64,8 @@ def _lib(mutation: int = 0):
             lib.oracle_max_threads.restype = i
             lib.oracle_paged_decode.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, p]
             lib.oracle_paged_decode.restype = i
+            lib.oracle_chunk_o.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_double, p]
+            lib.oracle_chunk_o.restype = i
             _LIBS[mutation] = lib
         return _LIBS[mutation]
 
@@ -149,4 +151,31 @@ def paged_decode(query, k_cache, v_cache, block_tables, seq_lens, dtype: str = "
         1 if dtype == "fp16" else 0, out.ctypes.data)
     if rc != 0:
         raise RuntimeError(f"oracle_paged_decode failed with {rc}")
+    return out
+
+
+def chunk_o(q, k, v, h, g, chunk_size: int = 64, scale: float | None = None,
+            mutation: int = 0) -> np.ndarray:
+    """Chunked gated delta-rule output, float64 [B, T, H, V].
+
+    ``q, k`` [B, T, Hq, K], ``v`` [B, T, H, V], ``h`` [B, NC, H, K, V]: bf16
+    bit patterns (uint16); ``g`` float32 [B, T, H]; NC = ceil(T / chunk_size).
+    """
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    B, T, Hq, K = q.shape
+    H, V = v.shape[2], v.shape[3]
+    nc = (T + chunk_size - 1) // chunk_size
+    if k.shape != q.shape or v.shape[:2] != (B, T) or h.shape != (B, nc, H, K, V) \
+            or g.shape != (B, T, H):
+        raise ValueError("shapes do not match")
+    out = np.zeros((B, T, H, V), dtype=np.float64)
+    rc = _lib(mutation).oracle_chunk_o(q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                       h.ctypes.data, g.ctypes.data, B, T, Hq, H, K, V,
+                                       int(chunk_size), float(scale or 0.0), out.ctypes.data)
+    if rc != 0:
+        raise RuntimeError(f"oracle_chunk_o failed with {rc}")
     return out

@@ -232,3 +232,61 @@ PAGED_CONFIGS = {
 def f16_bits_to_f64(b: np.ndarray) -> np.ndarray:
     """IEEE half bit patterns (uint16) -> exact float64 values."""
     return np.ascontiguousarray(b, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+# ---------------------------------------------------- chunked delta-rule output
+# atrex-bench "chunk_delta_rule_output" (page #004, input.py _make_inputs):
+# q, k ~ 0.02 N(0,1) bf16 [B, T, Hq, K]; v ~ 0.02 N(0,1) bf16 [B, T, H, V];
+# h ~ 0.02 N(0,1) bf16 [B, NC, H, K, V]; g = -U[0,1) float32 [B, T, H].
+# Drawn here in the order q, k, v, h, g from one seeded generator.
+
+
+@dataclass(frozen=True)
+class ChunkWorkload:
+    """One chunk_delta_rule_output call: the page's shape-table parameters."""
+
+    name: str
+    token_count: int
+    num_v_heads: int
+    value_dim: int
+    num_q_heads: int
+    chunk_size: int = 64
+    key_dim: int = 128
+    batch_size: int = 1
+    seed: int = 0
+
+    @property
+    def num_chunks(self) -> int:
+        return (self.token_count + self.chunk_size - 1) // self.chunk_size
+
+    def algorithmic_bytes(self) -> int:
+        """q, k, v, h read once, g read once, out written once."""
+        B, T = self.batch_size, self.token_count
+        qk = 2 * B * T * self.num_q_heads * self.key_dim * 2
+        vo = 2 * B * T * self.num_v_heads * self.value_dim * 2
+        hh = B * self.num_chunks * self.num_v_heads * self.key_dim * self.value_dim * 2
+        return qk + vo + hh + B * T * self.num_v_heads * 4
+
+
+def make_chunk_inputs(w: ChunkWorkload):
+    rng = np.random.default_rng(w.seed)
+    B, T, Hq, H = w.batch_size, w.token_count, w.num_q_heads, w.num_v_heads
+    K, V = w.key_dim, w.value_dim
+    f = lambda *s: (rng.standard_normal(s, dtype=np.float32) * np.float32(0.02))  # noqa: E731
+    q = round_to_bf16_bits(f(B, T, Hq, K))
+    k = round_to_bf16_bits(f(B, T, Hq, K))
+    v = round_to_bf16_bits(f(B, T, H, V))
+    h = round_to_bf16_bits(f(B, w.num_chunks, H, K, V))
+    g = -rng.random((B, T, H), dtype=np.float32)
+    return {"q": q, "k": k, "v": v, "h": h, "g": g}
+
+
+# The page's shape table, rows #0-#15.
+CHUNK_CONFIGS = {
+    f"D{i}": ChunkWorkload(f"D{i}_t{t}_h{hv}_q{hq}", t, hv, 128, hq, seed=120 + i)
+    for i, (t, hv, hq) in enumerate([
+        (64, 32, 16), (128, 32, 16), (256, 32, 16), (512, 32, 16), (1024, 32, 16),
+        (2048, 32, 16), (4096, 32, 16), (8192, 32, 16), (704, 16, 8), (1024, 16, 8),
+        (2112, 16, 8), (4096, 16, 8), (8256, 16, 8), (4195, 32, 16), (11027, 32, 16),
+        (14807, 32, 16)])
+}
