@@ -30,8 +30,8 @@ if ROOT not in sys.path:
 
 import numpy as np  # noqa: E402
 
-from workloads import (C1, C2, C3, C4, C5, CONFIGS, PAGED_CONFIGS, make_inputs,  # noqa: E402
-                       make_paged_inputs, sample_rows)
+from workloads import (C1, C2, C3, C4, C5, CHUNK_CONFIGS, CONFIGS, PAGED_CONFIGS,  # noqa: E402
+                       make_inputs, make_paged_inputs, sample_rows)
 
 HEADLINE = C2
 METRIC = "varlen attn fwd TFLOP/s (4*sum(L^2)*H*D)"
@@ -251,6 +251,35 @@ def graph_us_per_call(fn, stream) -> float:
     return statistics.median(reps)
 
 
+def run_profile_chunk(args):
+    """Only the chunked delta-rule output on one of the page's shapes: warm-up
+    and timed calls with L2 flushed before each, for runs under a profiler."""
+    import torch
+
+    import variable_length_prefill_gb300 as vlp
+    dev = torch.device("cuda", 0)
+    vlp.load()
+    cw = CHUNK_CONFIGS[args.profile_chunk]
+    gen = torch.Generator(device=dev).manual_seed(cw.seed)
+    B, T, Hq, Hv = cw.batch_size, cw.token_count, cw.num_q_heads, cw.num_v_heads
+    rnd = lambda *sh: (torch.randn(*sh, device=dev, generator=gen) * 0.02).to(torch.bfloat16)  # noqa: E731
+    q, k, v = rnd(B, T, Hq, 128), rnd(B, T, Hq, 128), rnd(B, T, Hv, 128)
+    h = rnd(B, cw.num_chunks, Hv, 128, 128)
+    g = -torch.rand(B, T, Hv, device=dev, generator=gen)
+    out = torch.empty(B, T, Hv, 128, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    fn = lambda: vlp.chunk_delta_rule_output(q, k, v, h, g, out=out)  # noqa: E731
+    for _ in range(args.warmup):
+        fn()
+    durs = time_calls(fn, args.steps, flush, torch.cuda.current_stream(dev))
+    vlp.check()
+    us = statistics.median(durs) * 1e3
+    print(json.dumps({"profile": True, "workload": "chunk_o_" + cw.name, "steps": args.steps,
+                      "us_median": round(us, 2),
+                      "gbs_algorithmic": round(cw.algorithmic_bytes() / (us * 1e-6) / 1e9, 1)}),
+          flush=True)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -382,6 +411,26 @@ def run_ours(args, rank, world, local_rank):
                 "pct_hbm": round(100.0 * pw.algorithmic_bytes() / (us * 1e-6) / 1e9 /
                                  peaks["hbm_gbs"], 2)}
         vlp.check()
+        # chunked gated delta-rule output: the page's shape table, HBM-bound;
+        # inputs drawn on the device with the test recipe's distributions
+        for name, cw in CHUNK_CONFIGS.items():
+            gen = torch.Generator(device=dev).manual_seed(cw.seed)
+            B, T, Hq, Hv = cw.batch_size, cw.token_count, cw.num_q_heads, cw.num_v_heads
+            rnd = lambda *sh: (torch.randn(*sh, device=dev, generator=gen) * 0.02).to(torch.bfloat16)  # noqa: E731
+            cq_, ck_, cv_ = rnd(B, T, Hq, 128), rnd(B, T, Hq, 128), rnd(B, T, Hv, 128)
+            ch_ = rnd(B, cw.num_chunks, Hv, 128, 128)
+            cg_ = -torch.rand(B, T, Hv, device=dev, generator=gen)
+            co_ = torch.empty(B, T, Hv, 128, dtype=torch.bfloat16, device=dev)
+            fn = lambda: vlp.chunk_delta_rule_output(cq_, ck_, cv_, ch_, cg_, out=co_)  # noqa: E731
+            for _ in range(3):
+                fn()
+            us = statistics.median(time_calls(fn, 20, flush, stream)) * 1e3
+            gbs = cw.algorithmic_bytes() / (us * 1e-6) / 1e9
+            shapes["chunk_o_" + cw.name] = {
+                "us": round(us, 2), "gbs_algorithmic": round(gbs, 1),
+                "pct_hbm": round(100.0 * gbs / peaks["hbm_gbs"], 2)}
+            del cq_, ck_, cv_, ch_, cg_, co_
+        vlp.check()
 
     if rank != 0:
         return
@@ -428,6 +477,8 @@ def main():
                     help="time this workload instead of the headline one")
     ap.add_argument("--profile", action="store_true",
                     help="warm-up and timed steps only, for runs under a profiler")
+    ap.add_argument("--profile-chunk", choices=sorted(CHUNK_CONFIGS), default=None,
+                    help="time only the chunked delta-rule output on this shape (profiler runs)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -436,6 +487,9 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.profile_chunk:
+        run_profile_chunk(args)
         return
     if world > 1:
         import torch.distributed as dist

@@ -19,7 +19,8 @@ def _declared():
     for f in sorted(os.listdir(INCLUDE)):
         if f.endswith(".h"):
             src = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, f)).read(), flags=re.S)
-            names |= set(re.findall(r"\b((?:attn_varlen|paged_attn)_\w+)\s*\(", src))
+            names |= set(re.findall(r"\b((?:attn_varlen|paged_attn|chunk_delta_rule)_\w+)\s*\(",
+                                    src))
     return names
 
 
@@ -124,3 +125,17 @@ def test_product_path_has_no_oracle_dependency():
 ])
 def test_paged_argument_checks_need_no_gpu(args, code):
     assert vlp.load().paged_attn_decode(*args) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    # (q, k, v, h, g, B, T, Hq, Hv, K, V, cs, scale, out)
+    ((P, P, P, P, P, -1, 64, 2, 4, 128, 128, 64, 0.0, P, None), B.ERR_INVALID_ARG),
+    ((P, P, P, P, P, 1, 64, 2, 4, 64, 128, 64, 0.0, P, None), B.ERR_UNSUPPORTED_DIM),
+    ((P, P, P, P, P, 1, 64, 2, 4, 128, 128, 32, 0.0, P, None), B.ERR_INVALID_ARG),
+    ((None, P, P, P, P, 1, 64, 2, 4, 128, 128, 64, 0.0, P, None), B.ERR_INVALID_ARG),
+    ((P, P, P + 8, P, P, 1, 64, 2, 4, 128, 128, 64, 0.0, P, None), B.ERR_MISALIGNED),
+    ((P, P, P, P, P + 2, 1, 64, 2, 4, 128, 128, 64, 0.0, P, None), B.ERR_MISALIGNED),
+    ((None, None, None, None, None, 1, 0, 2, 4, 128, 128, 64, 0.0, None, None), B.OK),
+])
+def test_chunk_argument_checks_need_no_gpu(args, code):
+    assert vlp.load().chunk_delta_rule_output(*args) == code

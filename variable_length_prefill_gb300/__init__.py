@@ -6,11 +6,14 @@ non-causal (or, as an option, causal), bf16 in and out.  It runs in a
 hand-written sm_103a CUDA library (TMA, tcgen05 MMA into TMEM,
 warp-specialised online softmax) behind the C ABI in include/attn_varlen.h;
 the same library holds the paged single-query decode of
-include/paged_attn_decode.h.  This package is a thin ctypes binding.
+include/paged_attn_decode.h and the chunked gated delta-rule output of
+include/chunk_delta_rule.h.  This package is a thin ctypes binding.
 """
 from ._binding import (AttnVarlenError, SYMBOLS, attn_varlen_fwd, attn_varlen_fwd_noalloc,
-                       check, load, paged_attn_decode, strerror, workspace_size)
+                       check, chunk_delta_rule_output, load, paged_attn_decode, strerror,
+                       workspace_size)
 from .build import build, lib_path
 
 __all__ = ["AttnVarlenError", "SYMBOLS", "attn_varlen_fwd", "attn_varlen_fwd_noalloc", "build",
-           "check", "lib_path", "load", "paged_attn_decode", "strerror", "workspace_size"]
+           "check", "chunk_delta_rule_output", "lib_path", "load", "paged_attn_decode", "strerror",
+           "workspace_size"]

@@ -40,6 +40,8 @@ SYMBOLS = {
     "attn_varlen_last_cuda_error": (ctypes.c_char_p, []),
     "attn_varlen_fwd_causal": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "paged_attn_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "chunk_delta_rule_output": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                     ctypes.c_float, _P, _P]),
 }
 
 _LOCK = threading.Lock()
@@ -218,4 +220,35 @@ def paged_attn_decode(query, k_cache, v_cache, block_tables, seq_lens, out=None,
                                    1 if query.dtype == torch.float16 else 0, out.data_ptr(), s)
     if rc != OK:
         raise AttnVarlenError(rc, "paged_attn_decode")
+    return out
+
+
+def chunk_delta_rule_output(q, k, v, h, g, chunk_size=64, scale=None, out=None, stream=None):
+    """Chunked gated delta-rule output (include/chunk_delta_rule.h).
+
+    q, k bf16 [B, T, Hq, 128]; v bf16 [B, T, Hv, 128]; h bf16
+    [B, ceil(T / 64), Hv, 128, 128]; g float32 [B, T, Hv]; all contiguous CUDA
+    tensors on one device.  Returns ``out`` (bf16 [B, T, Hv, 128]).
+    """
+    import torch
+    B, T, hq, kd = q.shape
+    hv, vd = v.shape[2], v.shape[3]
+    if out is None:
+        out = torch.empty((B, T, hv, vd), dtype=torch.bfloat16, device=q.device)
+    for name, t in (("q", q), ("k", k), ("v", v), ("h", h), ("out", out)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous bf16 tensor on {q.device}")
+    if g.dtype != torch.float32 or not g.is_contiguous() or g.device != q.device:
+        raise ValueError(f"g must be a contiguous float32 tensor on {q.device}")
+    if k.shape != q.shape or v.shape[:2] != (B, T) or g.shape != (B, T, hv) \
+            or h.shape != (B, (T + chunk_size - 1) // chunk_size, hv, kd, vd):
+        raise ValueError("shapes do not match")
+    lib = load()
+    s = _stream_handle(stream, q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.chunk_delta_rule_output(q.data_ptr(), k.data_ptr(), v.data_ptr(), h.data_ptr(),
+                                         g.data_ptr(), B, T, hq, hv, kd, vd, int(chunk_size),
+                                         float(scale or 0.0), out.data_ptr(), s)
+    if rc != OK:
+        raise AttnVarlenError(rc, "chunk_delta_rule_output")
     return out

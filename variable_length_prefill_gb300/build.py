@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libattn_varlen.so"
-SOURCES = ["attn_varlen_api.cu", "attn_varlen_kernels.cu", "paged_decode.cu"]
+SOURCES = ["attn_varlen_api.cu", "attn_varlen_kernels.cu", "paged_decode.cu", "chunk_o.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
               "-I", INCLUDE, "-I", CSRC]

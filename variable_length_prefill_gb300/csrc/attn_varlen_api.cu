@@ -13,6 +13,8 @@
 
 #include "attn_varlen.h"
 #include "attn_varlen_internal.h"
+#include "chunk_delta_rule.h"
+#include "chunk_o_internal.h"
 #include "paged_attn_decode.h"
 #include "paged_decode_internal.h"
 
@@ -378,6 +380,45 @@ int paged_attn_decode(const void* query, const void* k_cache, const void* v_cach
   p.num_blocks = num_blocks;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_size));
   return map_cuda(avp::launch_paged_decode(p, dtype == PAGED_ATTN_FP16, stream));
+}
+
+int chunk_delta_rule_output(const void* q, const void* k, const void* v, const void* h,
+                            const float* g, int batch, int tokens, int num_q_heads,
+                            int num_v_heads, int key_dim, int value_dim, int chunk_size,
+                            float scale, void* out, cudaStream_t stream) {
+  if (batch < 0 || tokens < 0 || num_q_heads < 1 || num_v_heads < 1)
+    return ATTN_VARLEN_ERR_INVALID_ARG;
+  if (key_dim != 128 || value_dim != 128) return ATTN_VARLEN_ERR_UNSUPPORTED_DIM;
+  if (chunk_size != 64) return ATTN_VARLEN_ERR_INVALID_ARG;
+  if (batch == 0 || tokens == 0) return ATTN_VARLEN_OK;
+  if (!q || !k || !v || !h || !g || !out) return ATTN_VARLEN_ERR_INVALID_ARG;
+  auto a16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+  if (!a16(q) || !a16(k) || !a16(v) || !a16(h) || !a16(out) ||
+      (reinterpret_cast<uintptr_t>(g) & 3u))
+    return ATTN_VARLEN_ERR_MISALIGNED;
+  int dev = 0;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if ((rc = probe_device(dev, st))) return rc;
+  if ((rc = get_encoder())) return rc;
+  if ((rc = ensure_workspace(st, 256))) return rc;  // the status word
+  avp::ChunkParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.h = h;
+  p.g = g;
+  p.out = out;
+  p.batch = batch;
+  p.tokens = tokens;
+  p.num_q_heads = num_q_heads;
+  p.num_v_heads = num_v_heads;
+  p.status = static_cast<int*>(st.ws);
+  p.sm_count = st.sm_count;
+  p.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)key_dim));
+  return map_cuda(avp::launch_chunk_o(p, g_encode, stream));
 }
 
 int attn_varlen_check(cudaStream_t stream) {
