@@ -42,11 +42,18 @@ NOMINAL_BF16_TFLOPS = 2250.0  # GB300 dense bf16, nominal (context; the roofline
 GRAPH_CALLS = 20              # calls per CUDA-graph replay for the launch-bound workload
 
 
+# The sources that build, plan and launch attn_varlen_fwd_kernel (the paged
+# decode and chunked delta-rule kernels live in translation units of their own
+# and cannot change it).
+ATTN_KERNEL_SOURCES = ("attn_varlen_api.cu", "attn_varlen_internal.h", "attn_varlen_kernels.cu",
+                       "ptx.cuh")
+
+
 def kernel_source_sha() -> str:
     import hashlib
     csrc = os.path.join(ROOT, "variable_length_prefill_gb300", "csrc")
     h = hashlib.sha256()
-    for n in sorted(os.listdir(csrc)):
+    for n in ATTN_KERNEL_SOURCES:
         h.update(n.encode())
         with open(os.path.join(csrc, n), "rb") as f:
             h.update(f.read())
