@@ -26,6 +26,7 @@ struct DeviceState {
   bool probed = false;
   bool supported = false;
   bool prepared[129] = {};  // kernel attributes set, by head_dim
+  bool chunk_prepared = false;  // the chunk-output kernel's attribute set
   int sm_count = 0;
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -415,6 +416,10 @@ int chunk_delta_rule_output(const void* q, const void* k, const void* v, const v
   p.tokens = tokens;
   p.num_q_heads = num_q_heads;
   p.num_v_heads = num_v_heads;
+  if (!st.chunk_prepared) {
+    if ((rc = map_cuda(avp::prepare_chunk_o()))) return rc;
+    st.chunk_prepared = true;
+  }
   p.status = static_cast<int*>(st.ws);
   p.sm_count = st.sm_count;
   p.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)key_dim));

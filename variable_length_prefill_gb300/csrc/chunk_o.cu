@@ -409,14 +409,11 @@ int encode(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, int rank, const c
 
 size_t chunk_o_smem_bytes() { return kSmemBytes; }
 
+cudaError_t prepare_chunk_o() {
+  return cudaFuncSetAttribute(chunk_o_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
 cudaError_t launch_chunk_o(const ChunkParams& p, EncodeTiledFn enc, cudaStream_t stream) {
-  static bool attr_set = false;  // per process; the attribute is per function, not per device
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_o_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   const long long nc = (p.tokens + kCs - 1) / kCs;
   const long long npairs = (nc + 1) / 2;
   const long long items = (long long)p.batch * p.num_v_heads * npairs;

@@ -31,8 +31,12 @@ struct ChunkParams {
 constexpr int kChunkStatusTimeout = 32;
 
 size_t chunk_o_smem_bytes();
-// Encodes the kernel's tensor maps with `enc` and launches.  Returns a CUDA
-// error, or cudaErrorInvalidValue when a map cannot be encoded.
+// Opts the kernel into its dynamic shared memory on the current device; once
+// per device before the first launch there.
+cudaError_t prepare_chunk_o();
+// Encodes the kernel's tensor maps with `enc` and launches on the current
+// device.  Returns a CUDA error, or cudaErrorInvalidValue when a map cannot
+// be encoded.
 cudaError_t launch_chunk_o(const ChunkParams& p, EncodeTiledFn enc, cudaStream_t stream);
 
 }  // namespace avp
