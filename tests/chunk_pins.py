@@ -125,5 +125,19 @@ def pin_head_map(mutation=0):
     assert np.all(np.abs(out[:, :, :2]).max(axis=-1) > 0)
 
 
+def pin_head_map_clamped(mutation=0):
+    """H = 6 value heads over Hq = 4: H / Hq rounds down to 1, so value head
+    hd reads q/k head min(hd, 3); heads 3, 4 and 5 all read head 3.  With
+    q/k heads 0-2 zero, value heads 0-2 are zero and 3-5 are not."""
+    rng = np.random.default_rng(96)
+    B, T, Hq, H, K, V, cs = 1, 5, 4, 6, 8, 4, 4
+    x = _inputs(rng, B, T, Hq, H, K, V, cs)
+    x["q"][:, :, :3] = 0
+    x["k"][:, :, :3] = 0
+    out = _run(x, cs, mutation)
+    assert np.all(out[:, :, :3] == 0.0)
+    assert np.all(np.abs(out[:, :, 3:]).max(axis=-1) > 0)
+
+
 CHUNK_PINS = [pin_state_only, pin_intra_only, pin_gate_mask,
-              pin_chunk_independence_and_padding, pin_head_map]
+              pin_chunk_independence_and_padding, pin_head_map, pin_head_map_clamped]
