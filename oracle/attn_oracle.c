@@ -156,6 +156,10 @@ int oracle_attn_varlen(const uint16_t* q, const uint16_t* k, const uint16_t* v,
         int64_t q0 = cu_q[i], Lq = (int64_t)cu_q[i + 1] - cu_q[i];
         int64_t k0 = MUT(4) ? cu_q[i] : cu_k[i];
         int64_t Lk = (int64_t)cu_k[i + 1] - cu_k[i];
+        if (MUT(13)) {  /* planted: a backwards slice read as the reversed range */
+            if (Lq < 0) { q0 = cu_q[i + 1]; Lq = -Lq; }
+            if (Lk < 0) { k0 = cu_k[i + 1]; Lk = -Lk; }
+        }
         if (Lq <= 0) continue;
         if (Lk < 0) Lk = 0;
         int64_t n = Lq * H;

@@ -220,6 +220,38 @@ def pin_empty_and_offsets(mutation=0):
     np.testing.assert_array_equal(out[cu_q[2]:cu_q[3]], 0.0)
 
 
+def pin_negative_slices(mutation=0):
+    """cu_seqlens that step backwards.  A negative query slice is skipped like
+    an empty one (the page's loop runs only while the query length is
+    positive), and a negative key slice is an empty key set, so its query rows
+    are zeros.  The live sequences must match torch float64 SDPA run on their
+    slices alone, and rows no live query slice covers keep the fill value.
+
+    cu_q = [20, 30, 25, 0, 10, 18] gives the query slices [20, 30), [30, 25),
+    [25, 0), [0, 10) and [10, 18); cu_k = [0, 50, 40, 60, 5, 33] gives the key
+    slices [0, 50), [50, 40), [40, 60), [60, 5) and [5, 33).  So sequences 1
+    and 2 are skipped, sequence 3 has a negative key slice, and rows 18, 19
+    and 30-39 belong to no sequence."""
+    import torch
+    rng = np.random.default_rng(24)
+    H, D = 2, 8
+    cu_q = np.array([20, 30, 25, 0, 10, 18], np.int32)
+    cu_k = np.array([0, 50, 40, 60, 5, 33], np.int32)
+    q = _rand_bits(rng, (40, H, D))
+    k = _rand_bits(rng, (70, H, D))
+    v = _rand_bits(rng, (70, H, D))
+    out = _run(q, k, v, cu_q, cu_k, mutation)
+    qf, kf, vf = (torch.from_numpy(bf16_bits_to_f64(x)) for x in (q, k, v))
+    for qs, ks in ((slice(20, 30), slice(0, 50)), (slice(10, 18), slice(5, 33))):
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qf[qs].transpose(0, 1)[None], kf[ks].transpose(0, 1)[None],
+            vf[ks].transpose(0, 1)[None])
+        np.testing.assert_allclose(out[qs], ref[0].transpose(0, 1).numpy(), rtol=0,
+                                   atol=1e-10)
+    np.testing.assert_array_equal(out[0:10], 0.0)
+    assert np.isnan(out[18:20]).all() and np.isnan(out[30:40]).all()
+
+
 def pin_torch_sdpa(mutation=0):
     """torch's CPU scaled_dot_product_attention in float64, per sequence and
     with its default scale, is an independent implementation of the same
@@ -352,6 +384,6 @@ def pin_causal_rows_match_full(mutation=0):
 PINS = [pin_single_key, pin_constant_keys, pin_zero_query, pin_equal_values,
         pin_two_keys, pin_key_permutation, pin_key_translation,
         pin_value_affine, pin_row_independence, pin_head_independence,
-        pin_packing, pin_empty_and_offsets, pin_torch_sdpa, pin_rows_match_full,
+        pin_packing, pin_empty_and_offsets, pin_negative_slices, pin_torch_sdpa, pin_rows_match_full,
         pin_causal_first_and_last_row, pin_causal_torch_sdpa, pin_causal_bottom_right,
         pin_causal_rows_match_full]

@@ -21,7 +21,8 @@ def test_pin(pin):
 #  6 the last key dropped                7 V row of the query token
 #  9 sign of the exponent flipped       10 NaN instead of zeros for L_k = 0
 # 11 causal: the diagonal key dropped   12 causal: mask aligned top-left
-MUTATIONS = [1, 3, 4, 5, 6, 7, 9, 10, 11, 12]
+# 13 a backwards cu_seqlens slice read as the reversed range
+MUTATIONS = [1, 3, 4, 5, 6, 7, 9, 10, 11, 12, 13]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS)
