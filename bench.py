@@ -3,8 +3,10 @@
 
 One step = one call of the whole path (plan kernel + fused attention kernel)
 over one batch of synthetic input resident in HBM.  The headline workload is
-one sequence L=8136, 16 heads, head_dim 72 (attention_forward shape-table
-row #4); the line also carries every workload's microseconds and TFLOP/s
+the largest one that fits one GPU: one sequence L=65556, 16 heads, head_dim
+72 (attention_forward shape-table row #8).  The line also carries a second
+full record for L=16742, 32 heads, head_dim 128 (row #9) under "records",
+and every workload's microseconds (median, p10, p90), TFLOP/s and SM clock
 under "shapes".  Metric: TFLOP/s with FLOPs = 4 * sum(L_q * L_k) * H * D
 (true head_dim).
 
@@ -33,7 +35,8 @@ import numpy as np  # noqa: E402
 from workloads import (C1, C2, C3, C4, C5, CHUNK_CONFIGS, CONFIGS, PAGED_CONFIGS,  # noqa: E402
                        make_inputs, make_paged_inputs, sample_rows)
 
-HEADLINE = C2
+HEADLINE = C4
+SECOND = C3  # the other full record (the dense head_dim-128 shape)
 METRIC = "varlen attn fwd TFLOP/s (4*sum(L^2)*H*D)"
 PAGE_TPROD_TFLOPS = {  # the page's T_Prod converted with the same FLOP count
     C1.name: 2.0, C2.name: 80.5, C3.name: 123.1, C4.name: 83.3}
@@ -86,11 +89,16 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle sampling while the timed region runs."""
+    """nvidia-smi clock/throttle sampling while the timed regions run.
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Every sample carries nvidia-smi's timestamp, so one sampler can cover
+    several timed legs: ``window(t0, t1)`` summarises the samples taken
+    between two ``time.time()`` readings."""
+
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -119,34 +127,53 @@ class ClockSampler:
                 self.proc.kill()
             self.f.close()
 
-    def summary(self):
+    def samples(self):
+        """[(epoch seconds or None, sm MHz, max MHz, set of active reasons)]"""
+        import datetime
+        out = []
         if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sms, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            return out
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm, smax = float(parts[1]), float(parts[2])
+                    sm, smax = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                sms.append(sm)
-                mx = smax
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
-        busy = [s for s in sms if mx and s > 0.3 * mx] or sms
-        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sms)}
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    ts = None
+                reasons = {n for n, v in zip(self.REASONS, parts[6:10]) if v.lower() == "active"}
+                out.append((ts, sm, smax, reasons))
+        return out
+
+    def summary(self, t0: float | None = None, t1: float | None = None):
+        """Median SM clock under load, max clock, p10/p90 and throttle reasons
+        of the samples in [t0, t1] (all samples without a window)."""
+        smp = self.samples()
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        if t0 is not None:
+            smp = [x for x in smp if x[0] is not None and t0 <= x[0] <= t1]
+        if not smp:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        mx = smp[-1][2]
+        sms = [x[1] for x in smp]
+        busy = sorted(s for s in sms if s > 0.3 * mx) or sorted(sms)
+        reasons = set().union(*(x[3] for x in smp))
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx,
+                "sm_mhz_p10": busy[len(busy) // 10], "sm_mhz_p90": busy[(9 * len(busy)) // 10],
+                "reasons": sorted(reasons), "samples": len(smp)}
 
 
-def cpu_oracle_rate(w, max_seconds=12.0, nthreads=0):
-    """Oracle throughput on a bounded, seeded sample of rows of workload w."""
+def cpu_oracle_rate(w, max_seconds=12.0, nthreads=0, x=None):
+    """Oracle throughput on a bounded, seeded sample of rows of workload w
+    (``x``: its inputs, when already drawn)."""
     import oracle
-    x = make_inputs(w)
+    x = make_inputs(w) if x is None else x
     rows_all = sample_rows(w, 4096, seed_offset=2000)
     cu = x["cu_q"]
     # rows of one head, all keys of their sequence: time a growing sample
@@ -175,11 +202,12 @@ def run_reference(args, rank, world):
     keys each), sized so that warm-up plus timed steps take about a minute."""
     if rank != 0:
         return
-    w = HEADLINE
+    w = CONFIGS[args.workload] if args.workload else HEADLINE
+    x = make_inputs(w)
     per_step = min(5.0, max(0.2, 60.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
-        cpu_oracle_rate(w, max_seconds=per_step)
-    runs = [cpu_oracle_rate(w, max_seconds=per_step) for _ in range(args.steps)]
+        cpu_oracle_rate(w, max_seconds=per_step, x=x)
+    runs = [cpu_oracle_rate(w, max_seconds=per_step, x=x) for _ in range(args.steps)]
     flops = sum(r["tflops"] * r["seconds"] for r in runs)
     secs = sum(r["seconds"] for r in runs)
     val = flops / secs if secs > 0 else 0.0
@@ -188,8 +216,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": secs / max(args.steps, 1) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "seq_lens": list(w.seq_lens_q),
-                       "num_heads": w.num_heads, "head_dim": w.head_dim},
+            "config": workload_config(w),
             "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": runs[0]["cores"] if runs else None,
                              "kind": "oracle",
                              "sample": f"{rows} seeded (token, head) rows of {w.name}, all keys "
@@ -287,6 +314,51 @@ def run_profile_chunk(args):
           flush=True)
 
 
+def workload_config(w) -> dict:
+    """The JSON line's config for workload w (both arms print the same)."""
+    return {"workload": w.name, "seq_lens": list(w.seq_lens_q), "num_heads": w.num_heads,
+            "head_dim": w.head_dim, "l2": "flushed before every step (256 MiB write)"}
+
+
+def percentiles_us(durs_ms) -> dict:
+    """Median, p10 and p90 of CUDA-event durations (ms) in microseconds."""
+    d = sorted(durs_ms)
+    return {"us": round(statistics.median(d) * 1e3, 2), "us_p10": round(d[len(d) // 10] * 1e3, 2),
+            "us_p90": round(d[(9 * len(d)) // 10] * 1e3, 2), "calls": len(d)}
+
+
+def timed_leg(fn, min_calls, flush_buf, stream, min_seconds=0.25):
+    """CUDA-event durations (ms) of at least ``min_calls`` calls, repeated
+    until the leg also spans ``min_seconds`` of wall time (so the clock
+    sampler sees it), with its (start, end) wall-clock times."""
+    import torch
+    t0 = time.time()
+    durs = []
+    while True:
+        durs += time_calls(fn, min_calls, flush_buf, stream)
+        if time.time() - t0 >= min_seconds:
+            break
+    torch.cuda.synchronize()
+    return durs, (t0, time.time())
+
+
+def clock_entry(c: dict) -> dict:
+    return {"sm_mhz": c.get("sm_mhz"), "sm_mhz_p10": c.get("sm_mhz_p10"),
+            "sm_mhz_p90": c.get("sm_mhz_p90"), "reasons": c.get("reasons"),
+            "samples": c.get("samples")}
+
+
+def roofline_block(w, per_call_tflops, peaks, kernel):
+    return {"bound": "tensor", "achieved": round(per_call_tflops, 2),
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(per_call_tflops / peaks["bf16_tflops"], 4),
+            "frac_of_nominal_2250": round(per_call_tflops / NOMINAL_BF16_TFLOPS, 4),
+            "traffic": measured_traffic(w.name),
+            "algorithmic_bytes": w.algorithmic_bytes(),
+            "peak_source": peaks["source"] + " bf16 burst",
+            "kernel": kernel}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -303,6 +375,9 @@ def run_ours(args, rank, world, local_rank):
         t = {n: torch.from_numpy(x[n].view(np.int16)).view(torch.bfloat16).to(dev)
              for n in ("q", "k", "v")}
         return x, t, torch.from_numpy(x["cu_q"]).to(dev), torch.from_numpy(x["cu_k"]).to(dev)
+
+    def kernel_name(w):
+        return (f"attn_varlen_fwd_kernel<{w.head_dim}> (+ plan kernel in the timed call)")
 
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     w = CONFIGS[args.workload] if args.workload else HEADLINE
@@ -357,107 +432,137 @@ def run_ours(args, rank, world, local_rank):
     e2e_durs = time_calls(e2e_step, e2e_steps, None, stream)
     e2e_value = whole_job_throughput(flops, e2e_steps, world,
                                      max_over_ranks(sum(e2e_durs) / 1e3, dev))
+    del dq, dk, dv, host, hout
 
-    # every workload once more: microseconds per call with L2 flushed before
-    # each call (cold) and without (warm), TFLOP/s of the cold time; for the
-    # launch-bound C1 also the time per call inside a replayed CUDA graph
-    shapes = {}
+    # The second full record and every workload once more, under one clock
+    # sampler: microseconds per call (median, p10, p90) with L2 flushed
+    # before each call (cold) and without (warm), the SM clock of each leg,
+    # and cycles per call (us x MHz) to separate clock drift from cache
+    # effects; for the launch-bound C1 also the time per call inside a
+    # replayed CUDA graph.
+    records, shapes = {}, {}
     if not args.headline_only:
-        for ws in (C1, C2, C3, C4, C5):
-            xs, ts, cq, ck = device_inputs(ws)
-            os_ = torch.empty_like(ts["q"])
-            fn = lambda: vlp.attn_varlen_fwd(ts["q"], ts["k"], ts["v"], cq, ck, out=os_)  # noqa: E731
-            for _ in range(3):
-                fn()
-            n = 5 if ws is C4 else 20
-            us = statistics.median(time_calls(fn, n, flush, stream)) * 1e3
-            us_warm = statistics.median(time_calls(fn, n, None, stream)) * 1e3
-            tf = ws.flops() / (us * 1e-6) / 1e12
-            entry = {"us": round(us, 2), "us_warm_l2": round(us_warm, 2), "tflops": round(tf, 2),
-                     "pct_bf16_peak": round(100.0 * tf / peaks["bf16_tflops"], 2),
-                     "pct_nominal_2250": round(100.0 * tf / NOMINAL_BF16_TFLOPS, 2),
-                     "gbs_algorithmic": round(ws.algorithmic_bytes() / (us * 1e-6) / 1e9, 1),
-                     "page_tprod_tflops": PAGE_TPROD_TFLOPS.get(ws.name)}
-            if ws is C1:
-                entry["us_per_call_in_graph"] = round(graph_us_per_call(fn, stream), 2)
-            shapes[ws.name] = entry
-            del ts, os_
-        vlp.check()
-        # the causal variant of the same workloads (FLOPs of the visible pairs)
-        for ws in (C2, C3, C5):
-            xs, ts, cq, ck = device_inputs(ws)
-            os_ = torch.empty_like(ts["q"])
-            fn = lambda: vlp.attn_varlen_fwd(ts["q"], ts["k"], ts["v"], cq, ck, out=os_,  # noqa: E731
-                                             causal=True)
-            for _ in range(3):
-                fn()
-            us = statistics.median(time_calls(fn, 10, flush, stream)) * 1e3
-            vis = sum(int(np.clip(np.arange(a) + 1 + b - a, 0, b).sum())
-                      for a, b in zip(ws.seq_lens_q, ws.lens_k) if a > 0 and b > 0)
-            shapes[ws.name + "_causal"] = {
-                "us": round(us, 2), "tflops": round(4.0 * vis * ws.num_heads * ws.head_dim /
-                                                    (us * 1e-6) / 1e12, 2)}
-            del ts, os_
-        # paged single-query decode: the page's shape table, HBM-bound
-        for name, pw in PAGED_CONFIGS.items():
-            xs = make_paged_inputs(pw)
-            tdt = torch.bfloat16 if pw.dtype == "bf16" else torch.float16
-            pt = {n: torch.from_numpy(xs[n].view(np.int16)).view(tdt).to(dev)
-                  for n in ("query", "k_cache", "v_cache")}
-            tb = torch.from_numpy(xs["block_tables"]).to(dev)
-            ln = torch.from_numpy(xs["seq_lens"]).to(dev)
-            po = torch.empty_like(pt["query"])
-            fn = lambda: vlp.paged_attn_decode(pt["query"], pt["k_cache"], pt["v_cache"],  # noqa: E731
-                                               tb, ln, out=po)
-            for _ in range(3):
-                fn()
-            us = statistics.median(time_calls(fn, 20, flush, stream)) * 1e3
-            shapes["paged_" + pw.name] = {
-                "us": round(us, 2),
-                "gbs_algorithmic": round(pw.algorithmic_bytes() / (us * 1e-6) / 1e9, 1),
-                "pct_hbm": round(100.0 * pw.algorithmic_bytes() / (us * 1e-6) / 1e9 /
-                                 peaks["hbm_gbs"], 2)}
-        vlp.check()
-        # chunked gated delta-rule output: the page's shape table, HBM-bound;
-        # inputs drawn on the device with the test recipe's distributions
-        for name, cw in CHUNK_CONFIGS.items():
-            gen = torch.Generator(device=dev).manual_seed(cw.seed)
-            B, T, Hq, Hv = cw.batch_size, cw.token_count, cw.num_q_heads, cw.num_v_heads
-            rnd = lambda *sh: (torch.randn(*sh, device=dev, generator=gen) * 0.02).to(torch.bfloat16)  # noqa: E731
-            cq_, ck_, cv_ = rnd(B, T, Hq, 128), rnd(B, T, Hq, 128), rnd(B, T, Hv, 128)
-            ch_ = rnd(B, cw.num_chunks, Hv, 128, 128)
-            cg_ = -torch.rand(B, T, Hv, device=dev, generator=gen)
-            co_ = torch.empty(B, T, Hv, 128, dtype=torch.bfloat16, device=dev)
-            fn = lambda: vlp.chunk_delta_rule_output(cq_, ck_, cv_, ch_, cg_, out=co_)  # noqa: E731
-            for _ in range(3):
-                fn()
-            us = statistics.median(time_calls(fn, 20, flush, stream)) * 1e3
-            gbs = cw.algorithmic_bytes() / (us * 1e-6) / 1e9
-            shapes["chunk_o_" + cw.name] = {
-                "us": round(us, 2), "gbs_algorithmic": round(gbs, 1),
-                "pct_hbm": round(100.0 * gbs / peaks["hbm_gbs"], 2)}
-            del cq_, ck_, cv_, ch_, cg_, co_
-        vlp.check()
+        with ClockSampler(local_rank) as sampler:
+            if w is not SECOND:
+                xs, ts, cq, ck = device_inputs(SECOND)
+                os_ = torch.empty_like(ts["q"])
+                fn = lambda: vlp.attn_varlen_fwd(ts["q"], ts["k"], ts["v"], cq, ck, out=os_)  # noqa: E731
+                for _ in range(3):
+                    fn()
+                d2, win = timed_leg(fn, max(args.steps, 20), flush, stream)
+                vlp.check()
+                t2 = max_over_ranks(statistics.median(d2) / 1e3, dev)
+                tf2 = SECOND.flops() / t2 / 1e12
+                records[SECOND.name] = {
+                    "metric": METRIC, "value": round(tf2 * world, 3), "unit": "TFLOP/s",
+                    "ms_per_step": round(t2 * 1e3, 4), **percentiles_us(d2),
+                    "config": workload_config(SECOND),
+                    "roofline": roofline_block(SECOND, tf2, peaks, kernel_name(SECOND)),
+                    "clocks": clock_entry(sampler.summary(*win))}
+                del ts, os_
+            for ws in (C1, C2, C3, C4, C5):
+                xs, ts, cq, ck = device_inputs(ws)
+                os_ = torch.empty_like(ts["q"])
+                fn = lambda: vlp.attn_varlen_fwd(ts["q"], ts["k"], ts["v"], cq, ck, out=os_)  # noqa: E731
+                for _ in range(3):
+                    fn()
+                n = 10 if ws is C4 else 20
+                cold, win_c = timed_leg(fn, n, flush, stream)
+                warm, win_w = timed_leg(fn, n, None, stream)
+                pc, pw = percentiles_us(cold), percentiles_us(warm)
+                cc, cw_ = clock_entry(sampler.summary(*win_c)), clock_entry(sampler.summary(*win_w))
+                tf = ws.flops() / (pc["us"] * 1e-6) / 1e12
+                entry = {**pc, "tflops": round(tf, 2),
+                         "pct_bf16_peak": round(100.0 * tf / peaks["bf16_tflops"], 2),
+                         "pct_nominal_2250": round(100.0 * tf / NOMINAL_BF16_TFLOPS, 2),
+                         "gbs_algorithmic": round(ws.algorithmic_bytes() / (pc["us"] * 1e-6) / 1e9, 1),
+                         "page_tprod_tflops": PAGE_TPROD_TFLOPS.get(ws.name),
+                         "clocks": cc,
+                         "kcycles": round(pc["us"] * cc["sm_mhz"] / 1e3, 1) if cc["sm_mhz"] else None,
+                         "warm_l2": {**pw, "clocks": cw_,
+                                     "kcycles": round(pw["us"] * cw_["sm_mhz"] / 1e3, 1)
+                                     if cw_["sm_mhz"] else None}}
+                if ws is C1:
+                    entry["us_per_call_in_graph"] = round(graph_us_per_call(fn, stream), 2)
+                shapes[ws.name] = entry
+                del ts, os_
+            vlp.check()
+            # the causal variant of the same workloads (FLOPs of the visible pairs)
+            for ws in (C2, C3, C5):
+                xs, ts, cq, ck = device_inputs(ws)
+                os_ = torch.empty_like(ts["q"])
+                fn = lambda: vlp.attn_varlen_fwd(ts["q"], ts["k"], ts["v"], cq, ck, out=os_,  # noqa: E731
+                                                 causal=True)
+                for _ in range(3):
+                    fn()
+                d, win = timed_leg(fn, 10, flush, stream)
+                pc = percentiles_us(d)
+                vis = sum(int(np.clip(np.arange(a) + 1 + b - a, 0, b).sum())
+                          for a, b in zip(ws.seq_lens_q, ws.lens_k) if a > 0 and b > 0)
+                shapes[ws.name + "_causal"] = {
+                    **pc, "tflops": round(4.0 * vis * ws.num_heads * ws.head_dim /
+                                          (pc["us"] * 1e-6) / 1e12, 2),
+                    "clocks": clock_entry(sampler.summary(*win))}
+                del ts, os_
+            # paged single-query decode: the page's shape table, HBM-bound
+            for name, pw in PAGED_CONFIGS.items():
+                xs = make_paged_inputs(pw)
+                tdt = torch.bfloat16 if pw.dtype == "bf16" else torch.float16
+                pt = {n: torch.from_numpy(xs[n].view(np.int16)).view(tdt).to(dev)
+                      for n in ("query", "k_cache", "v_cache")}
+                tb = torch.from_numpy(xs["block_tables"]).to(dev)
+                ln = torch.from_numpy(xs["seq_lens"]).to(dev)
+                po = torch.empty_like(pt["query"])
+                fn = lambda: vlp.paged_attn_decode(pt["query"], pt["k_cache"], pt["v_cache"],  # noqa: E731
+                                                   tb, ln, out=po)
+                for _ in range(3):
+                    fn()
+                d, win = timed_leg(fn, 20, flush, stream, min_seconds=0.1)
+                pc = percentiles_us(d)
+                gbs = pw.algorithmic_bytes() / (pc["us"] * 1e-6) / 1e9
+                shapes["paged_" + pw.name] = {
+                    **pc, "gbs_algorithmic": round(gbs, 1),
+                    "pct_hbm": round(100.0 * gbs / peaks["hbm_gbs"], 2),
+                    "clocks": clock_entry(sampler.summary(*win))}
+            vlp.check()
+            # chunked gated delta-rule output: the page's shape table, HBM-bound;
+            # inputs drawn on the device with the test recipe's distributions
+            for name, cw in CHUNK_CONFIGS.items():
+                gen = torch.Generator(device=dev).manual_seed(cw.seed)
+                B, T, Hq, Hv = cw.batch_size, cw.token_count, cw.num_q_heads, cw.num_v_heads
+                rnd = lambda *sh: (torch.randn(*sh, device=dev, generator=gen) * 0.02).to(torch.bfloat16)  # noqa: E731
+                cq_, ck_, cv_ = rnd(B, T, Hq, 128), rnd(B, T, Hq, 128), rnd(B, T, Hv, 128)
+                ch_ = rnd(B, cw.num_chunks, Hv, 128, 128)
+                cg_ = -torch.rand(B, T, Hv, device=dev, generator=gen)
+                co_ = torch.empty(B, T, Hv, 128, dtype=torch.bfloat16, device=dev)
+                fn = lambda: vlp.chunk_delta_rule_output(cq_, ck_, cv_, ch_, cg_, out=co_)  # noqa: E731
+                for _ in range(3):
+                    fn()
+                d, win = timed_leg(fn, 20, flush, stream, min_seconds=0.1)
+                pc = percentiles_us(d)
+                gbs = cw.algorithmic_bytes() / (pc["us"] * 1e-6) / 1e9
+                shapes["chunk_o_" + cw.name] = {
+                    **pc, "gbs_algorithmic": round(gbs, 1),
+                    "pct_hbm": round(100.0 * gbs / peaks["hbm_gbs"], 2),
+                    "clocks": clock_entry(sampler.summary(*win))}
+                del cq_, ck_, cv_, ch_, cg_, co_
+            vlp.check()
 
     if rank != 0:
         return
-    cpu = cpu_oracle_rate(w, max_seconds=args.cpu_seconds)
-    cpu1 = cpu_oracle_rate(w, max_seconds=min(4.0, args.cpu_seconds), nthreads=1)
+    cpu = cpu_oracle_rate(w, max_seconds=args.cpu_seconds, x=x)
+    cpu1 = cpu_oracle_rate(w, max_seconds=min(4.0, args.cpu_seconds), nthreads=1, x=x)
+    tprod = PAGE_TPROD_TFLOPS.get(w.name)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": round(value / world / PAGE_TPROD_TFLOPS[w.name], 3),
+        # the page's T_Prod for this workload (other, unnamed hardware): context
+        "vs_baseline": round(value / world / tprod, 3) if tprod else None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "seq_lens": list(w.seq_lens_q), "num_heads": w.num_heads,
-                   "head_dim": w.head_dim, "l2": "flushed before every step (256 MiB write)"},
-        "roofline": {"bound": "tensor", "achieved": round(per_call_tflops, 2),
-                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(per_call_tflops / peaks["bf16_tflops"], 4),
-                     "traffic": measured_traffic(w.name),
-                     "algorithmic_bytes": w.algorithmic_bytes(),
-                     "peak_source": peaks["source"] + " bf16 burst",
-                     "kernel": "attn_varlen_fwd_kernel<72> (+ plan kernel in the timed call)"},
+        "config": workload_config(w),
+        **{k: v for k, v in percentiles_us(durs).items() if k != "us"},
+        "roofline": roofline_block(w, per_call_tflops, peaks, kernel_name(w)),
         "cpu_baseline": {"value": cpu["tflops"], "unit": "TFLOP/s", "cores": cpu["cores"],
                          "kind": "oracle", "rows_per_s": cpu["rows_per_s"],
                          "rows_per_s_1_thread": cpu1["rows_per_s"],
@@ -467,6 +572,7 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks.summary(),
+        "records": records,
         "shapes": shapes,
     }
     print(json.dumps(line), flush=True)

@@ -157,15 +157,27 @@ int attn_varlen_check_ws(void* workspace, cudaStream_t stream);
  * (once, with that device current); make that first call before any stream
  * capture.  Every call on a device shares the one array: calls that can
  * overlap on the GPU (different streams without ordering) race and give
- * wrong results, so order them.  Each call clears the array's status word
- * on `stream`; device-side wait timeouts of this variant are not reported
- * by attn_varlen_check.
+ * wrong results, so order them.  The array's first word is this variant's
+ * device status word: zero when the library loads, set by a kernel wait that
+ * timed out, kept across calls, and read and cleared only by
+ * attn_varlen_check_noalloc (attn_varlen_check reads the library-owned
+ * workspace instead).
  */
 #define ATTN_VARLEN_NOALLOC_MAX_SEQS 1024
 int attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v,
                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                             int num_seqs, int num_heads, int head_dim, void* out,
                             cudaStream_t stream);
+
+/*
+ * attn_varlen_check_noalloc -- attn_varlen_check for the fixed scratch of
+ * attn_varlen_fwd_noalloc: synchronise `stream`, then read and clear that
+ * scratch's status word on the current device.  Returns ATTN_VARLEN_OK (also
+ * when attn_varlen_fwd_noalloc never ran on this device),
+ * ATTN_VARLEN_ERR_DEVICE_TIMEOUT when a kernel wait of a no-alloc call ran out
+ * of time since the last check, or ATTN_VARLEN_ERR_CUDA.  Allocates nothing.
+ */
+int attn_varlen_check_noalloc(cudaStream_t stream);
 
 /* Static, human-readable text for an ATTN_VARLEN_* code. */
 const char* attn_varlen_strerror(int code);

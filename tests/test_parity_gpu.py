@@ -83,6 +83,41 @@ def test_rows_outside_sequences_untouched(cuda_lib):
     assert_close(got[cu[0]:cu[-1]], ref[cu[0]:cu[-1]], "offsets")
 
 
+@pytest.mark.parametrize("D,causal,ws", [(72, False, False), (128, False, True),
+                                         (72, True, False), (128, True, False)])
+def test_backwards_cu_seqlens(cuda_lib, D, causal, ws):
+    """cu_seqlens that step backwards, every offset inside the buffers.  Query
+    slices [600, 900), [900, 750), [750, 0), [0, 300), [300, 540); key slices
+    [0, 1500), [1500, 1200), [1200, 1800), [1800, 150), [150, 990).  The two
+    backwards query slices are skipped, the backwards key slice of the fourth
+    sequence gives zero rows, and rows 540-599 and 900-999 belong to no
+    sequence: a sentinel there must survive bit for bit."""
+    from workloads import round_to_bf16_bits
+    rng = np.random.default_rng(48 + D)
+    H = 2
+    x = {"q": round_to_bf16_bits(rng.standard_normal((1000, H, D), dtype=np.float32)),
+         "k": round_to_bf16_bits(rng.standard_normal((2000, H, D), dtype=np.float32)),
+         "v": round_to_bf16_bits(rng.standard_normal((2000, H, D), dtype=np.float32)),
+         "cu_q": np.array([600, 900, 750, 0, 300, 540], np.int32),
+         "cu_k": np.array([0, 1500, 1200, 1800, 150, 990], np.int32)}
+    sentinel = 0x7FC1
+    if ws:
+        got = run_cuda(cuda_lib, x, out_fill=sentinel, caller_workspace=True)
+    else:
+        got = run_cuda(cuda_lib, x, out_fill=sentinel, causal=causal)
+    assert (got[540:600] == sentinel).all() and (got[900:] == sentinel).all()
+    assert (got[0:300] == 0).all()
+    ref = oracle.attn_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], causal=causal)
+    live = np.r_[300:540, 600:900]
+    bound = None
+    if causal:  # the first rows of a causal sequence average only a few values
+        absv = oracle.attn_varlen(x["q"], x["k"], abs_bits(x["v"]), x["cu_q"], x["cu_k"],
+                                  causal=True)
+        bound = bf16_bound(ref[live], absv[live])
+    assert_close(got[live], ref[live], f"backwards cu_seqlens D={D} causal={causal}",
+                 bound=bound)
+
+
 def test_num_seqs_zero_is_a_noop(cuda_lib):
     import torch
     q = torch.zeros(4, 2, 72, dtype=torch.bfloat16, device="cuda")

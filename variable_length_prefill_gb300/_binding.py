@@ -34,6 +34,7 @@ SYMBOLS = {
     "attn_varlen_fwd_ws": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _SZ, _P]),
     "attn_varlen_check": (_I, [_P]),
     "attn_varlen_check_ws": (_I, [_P, _P]),
+    "attn_varlen_check_noalloc": (_I, [_P]),
     "attn_varlen_strerror": (ctypes.c_char_p, [_I]),
     "attn_varlen_version": (_I, []),
     "attn_varlen_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
@@ -151,13 +152,18 @@ def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, out=None, stream=None,
     return out
 
 
-def check(stream=None, device=None, workspace=None) -> int:
-    """Synchronise and return (and clear) the device status; raises on error."""
+def check(stream=None, device=None, workspace=None, noalloc=False) -> int:
+    """Synchronise and return (and clear) the device status; raises on error.
+
+    ``workspace``: the caller-owned workspace to read; ``noalloc``: read the
+    status of attn_varlen_fwd_noalloc's fixed scratch instead."""
     import torch
     dev = device if device is not None else torch.cuda.current_device()
     s = _stream_handle(stream, dev)
     with torch.cuda.device(dev):
-        if workspace is None:
+        if noalloc:
+            rc = load().attn_varlen_check_noalloc(s)
+        elif workspace is None:
             rc = load().attn_varlen_check(s)
         else:
             rc = load().attn_varlen_check_ws(workspace.data_ptr(), s)

@@ -18,14 +18,23 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libattn_varlen.so"
+# Test-only builds: the same sources with extra defines, in a library of their
+# own that the product never loads.  "waittest" shortens every kernel wait to
+# 50 ms and compiles the hook that withholds one K/V tile, so a test can run
+# a wait out and check the reported status.
+VARIANTS = {
+    "waittest": ("libattn_varlen_waittest.so",
+                 ["-DATTN_VARLEN_WAIT_LIMIT_NS=50000000ull", "-DATTN_VARLEN_TEST_HOOKS=1"]),
+}
 SOURCES = ["attn_varlen_api.cu", "attn_varlen_kernels.cu", "paged_decode.cu", "chunk_o.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
               "-I", INCLUDE, "-I", CSRC]
 
 
-def lib_path() -> str:
-    return os.path.join(LIB_DIR, LIB_NAME)
+def lib_path(variant: str | None = None) -> str:
+    name = LIB_NAME if variant is None else VARIANTS[variant][0]
+    return os.path.join(LIB_DIR, name)
 
 
 def _nvcc() -> str:
@@ -35,33 +44,37 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build the library")
 
 
-def _fingerprint() -> str:
+def _fingerprint(extra: list) -> str:
     h = hashlib.sha256()
     for d in (CSRC, INCLUDE):
         for name in sorted(os.listdir(d)):
             with open(os.path.join(d, name), "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
-    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    h.update(" ".join(ARCH + NVCC_FLAGS + extra).encode())
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if sources changed) and return the library path."""
+def build(force: bool = False, verbose: bool = False, variant: str | None = None) -> str:
+    """Compile (if sources changed) and return the library path.
+
+    ``variant``: a key of VARIANTS to build that test-only library instead."""
     os.makedirs(LIB_DIR, exist_ok=True)
-    out = lib_path()
+    out = lib_path(variant)
+    extra = [] if variant is None else VARIANTS[variant][1]
     stamp = out + ".sha256"
-    fp = _fingerprint()
+    fp = _fingerprint(extra)
     if not force and os.path.exists(out) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == fp:
                 return out
     nvcc = _nvcc()
     objs, procs = [], []
+    tag = "" if variant is None else "_" + variant
     for src in SOURCES:
-        obj = os.path.join(LIB_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(LIB_DIR, src.replace(".cu", f"{tag}.o"))
         objs.append(obj)
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE,

@@ -48,6 +48,12 @@ bool g_encode_probed = false;
 // Last CUDA runtime error this library saw on the calling thread.
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
+#ifndef ATTN_VARLEN_TEST_HOOKS
+#define ATTN_VARLEN_TEST_HOOKS 0
+#endif
+// Set only through the test build's attn_varlen_test_withhold (FwdParams).
+int g_test_withhold = 0;
+
 int fail_cuda(cudaError_t e) {
   g_last_cuda_error = e;
   cudaGetLastError();  // do not leave the error pending for the caller
@@ -179,6 +185,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const 
   fp.num_heads = num_heads;
   fp.causal = causal ? 1 : 0;
   fp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
+  fp.test_withhold = g_test_withhold;
 
   const int slot = head_dim;
   if (!st.prepared[slot]) {
@@ -328,11 +335,10 @@ int attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v,
     if (!ptr) return ATTN_VARLEN_ERR_CUDA;
     g_noalloc_ptr[dev] = ptr;
   }
+  // The plan kernel rewrites everything the attention kernel reads.  The
+  // status word (zero when the module loads) is left alone: it is sticky
+  // until attn_varlen_check_noalloc reads and clears it.
   void* ws = g_noalloc_ptr[dev];
-  // the status word is the only part that must start at zero; the plan
-  // kernel rewrites everything else the attention kernel reads
-  cudaError_t me = cudaMemsetAsync(ws, 0, sizeof(int), stream);
-  if (me != cudaSuccess) return fail_cuda(me);
   return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, ws, 0, dev,
              st, stream);
 }
@@ -443,6 +449,28 @@ int attn_varlen_check_ws(void* workspace, cudaStream_t stream) {
   if (!workspace) return ATTN_VARLEN_ERR_INVALID_ARG;
   return read_and_clear_status(workspace, stream);
 }
+
+int attn_varlen_check_noalloc(cudaStream_t stream) {
+  int dev = 0;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    ws = g_noalloc_ptr[dev];
+  }
+  if (!ws) return map_cuda(cudaStreamSynchronize(stream));
+  return read_and_clear_status(ws, stream);
+}
+
+#if ATTN_VARLEN_TEST_HOOKS
+// Test builds only: make the next calls withhold one K/V tile (see
+// ATTN_VARLEN_TEST_HOOKS in attn_varlen_kernels.cu) so a bounded wait runs out.
+void attn_varlen_test_withhold(int on) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_test_withhold = on ? 1 : 0;
+}
+#endif
 
 const char* attn_varlen_strerror(int code) {
   switch (code) {

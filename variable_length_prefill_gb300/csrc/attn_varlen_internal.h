@@ -120,6 +120,7 @@ struct FwdParams {
   int num_heads;
   int causal;        // 1: row r of a sequence sees keys <= r + L_k - L_q
   float scale_log2;  // head_dim^-1/2 * log2(e)
+  int test_withhold; // read only by test builds (ATTN_VARLEN_TEST_HOOKS); 0 otherwise
 };
 
 // Kernel launchers (attn_varlen_kernels.cu).

@@ -83,7 +83,19 @@ constexpr float kRescaleThreshold = 8.0f;
 #define ATTN_VARLEN_STRICT_PV_WAIT 0
 #endif
 constexpr bool kStrictPvWait = ATTN_VARLEN_STRICT_PV_WAIT != 0;
-constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
+// Time after which a wait gives up.  The product build waits 4 s; a test
+// build shortens it to run the give-up path (see ATTN_VARLEN_TEST_HOOKS).
+#ifndef ATTN_VARLEN_WAIT_LIMIT_NS
+#define ATTN_VARLEN_WAIT_LIMIT_NS 4000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = ATTN_VARLEN_WAIT_LIMIT_NS;
+// Test builds only (never the product library): with FwdParams::test_withhold
+// set, CTA 0's producer neither issues nor announces its first K/V tile, so
+// the MMA warp's wait on that slot runs out and the give-up path (status
+// bit, abort flag, drain, TMEM free) runs with no copy in flight on it.
+#ifndef ATTN_VARLEN_TEST_HOOKS
+#define ATTN_VARLEN_TEST_HOOKS 0
+#endif
 #ifndef ATTN_VARLEN_TAIL_SPLIT
 #define ATTN_VARLEN_TAIL_SPLIT 1
 #endif
@@ -758,12 +770,17 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
         const uint32_t stage = kv_item % G::STAGES;
         const uint32_t use = kv_item / G::STAGES;
         if (!(ok = wait_(bar(G::B_KV_EMPTY + stage), (use & 1u) ^ 1u))) break;
-        mbar_arrive_expect_tx_if(leader, bar(G::B_KV_FULL + stage), G::KV_TILE_BYTES);
+#if ATTN_VARLEN_TEST_HOOKS
+        const uint32_t issue = (p.test_withhold && blockIdx.x == 0 && kv_item == 0) ? 0u : leader;
+#else
+        const uint32_t issue = leader;
+#endif
+        mbar_arrive_expect_tx_if(issue, bar(G::B_KV_FULL + stage), G::KV_TILE_BYTES);
         const uint8_t* m = is_v ? mv : mk;
         const uint32_t dst = sKV + stage * G::KV_TILE_BYTES;
 #pragma unroll
         for (int b = 0; b < G::NB; ++b)
-          tma_load_3d_if(leader, dst + b * G::KV_BOX_BYTES, m, bar(G::B_KV_FULL + stage),
+          tma_load_3d_if(issue, dst + b * G::KV_BOX_BYTES, m, bar(G::B_KV_FULL + stage),
                          b * G::BW, ui.head, (ui.jb + j) * G::KN);
         ++kv_item;
       }
