@@ -113,6 +113,19 @@ constexpr int kMergeTiles = 8;
 #define ATTN_VARLEN_KV_STAGES_128 4
 #endif
 
+// Share of the softmax's exponentials computed on the FMA pipe
+// (exp2_poly2) instead of the MUFU unit: POLY of every 7 groups of four
+// columns.  The MUFU unit retires 16 exponentials per clock per SM and
+// bounds the softmax of the small head dims; moving about 3/7 of them to
+// FMA arithmetic (about five issue slots each) balances the two.
+#ifndef ATTN_VARLEN_POLY_SMALL
+#define ATTN_VARLEN_POLY_SMALL 3
+#endif
+#ifndef ATTN_VARLEN_POLY_128
+#define ATTN_VARLEN_POLY_128 0
+#endif
+constexpr int kPolyDen = 7;
+
 // Per head_dim configuration.  Every head_dim other than 128 runs the
 // separate-P, two-issuer schedule; the key tile is the largest multiple of 16
 // whose S, P and O columns for two Q tiles fit the 512 TMEM columns
@@ -128,6 +141,7 @@ struct Cfg<64> {
   static constexpr int ISSUERS = 2;
   static constexpr int STAGES = 6;  // 16 KB per K or V tile
   static constexpr uint32_t SWZ = kSwizzle128B;
+  static constexpr int POLY = ATTN_VARLEN_POLY_SMALL;
 };
 template <>
 struct Cfg<80> {
@@ -138,6 +152,7 @@ struct Cfg<80> {
   static constexpr int ISSUERS = 2;
   static constexpr int STAGES = 4;
   static constexpr uint32_t SWZ = kSwizzle128B;
+  static constexpr int POLY = ATTN_VARLEN_POLY_SMALL;
 };
 template <>
 struct Cfg<96> {
@@ -148,6 +163,7 @@ struct Cfg<96> {
   static constexpr int ISSUERS = 2;
   static constexpr int STAGES = 4;
   static constexpr uint32_t SWZ = kSwizzle128B;
+  static constexpr int POLY = ATTN_VARLEN_POLY_SMALL;
 };
 template <>
 struct Cfg<72> {
@@ -159,6 +175,7 @@ struct Cfg<72> {
   static constexpr int ISSUERS = 2;   // one MMA-issuing warp per Q tile
   static constexpr int STAGES = ATTN_VARLEN_KV_STAGES_72;
   static constexpr uint32_t SWZ = kSwizzle128B;
+  static constexpr int POLY = ATTN_VARLEN_POLY_SMALL;
 };
 template <>
 struct Cfg<128> {
@@ -169,6 +186,7 @@ struct Cfg<128> {
   static constexpr int ISSUERS = 1;    // one MMA-issuing warp for both Q tiles
   static constexpr int STAGES = ATTN_VARLEN_KV_STAGES_128;
   static constexpr uint32_t SWZ = kSwizzle128B;
+  static constexpr int POLY = ATTN_VARLEN_POLY_128;
 };
 
 template <int D>
@@ -183,6 +201,8 @@ struct Geometry {
   static constexpr int NB = (DP + BW - 1) / BW;             // boxes per tile
   static constexpr int STAGES = Cfg<D>::STAGES;
   static constexpr uint32_t SWZ = Cfg<D>::SWZ;
+  static constexpr int POLY = Cfg<D>::POLY;
+  static_assert(POLY >= 0 && POLY <= kPolyDen, "polynomial share");
   static constexpr uint32_t Q_BOX_BYTES = kBlockM * BW * 2;  // one box: 128 rows x BW
   static constexpr uint32_t Q_TILE_BYTES = NB * Q_BOX_BYTES;
   static constexpr uint32_t KV_BOX_BYTES = KN * BW * 2;      // one box: KN keys x BW
@@ -1130,10 +1150,17 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
                                   c2, nm2);
             float2 b = __ffma2_rn(make_float2(__uint_as_float(s[2 * c + 2]),
                                               __uint_as_float(s[2 * c + 3])), c2, nm2);
-            a.x = ex2(a.x);
-            a.y = ex2(a.y);
-            b.x = ex2(b.x);
-            b.y = ex2(b.y);
+            // group c / 2 of four columns: FMA-pipe polynomial or MUFU
+            // (a compile-time choice once the loop is unrolled)
+            if (((c >> 1) * G::POLY) % kPolyDen < G::POLY) {
+              a = exp2_poly2(a);
+              b = exp2_poly2(b);
+            } else {
+              a.x = ex2(a.x);
+              a.y = ex2(a.y);
+              b.x = ex2(b.x);
+              b.y = ex2(b.y);
+            }
             acc0 = __fadd2_rn(acc0, a);
             acc1 = __fadd2_rn(acc1, b);
             pk[c] = pack_bf16x2(a.x, a.y);

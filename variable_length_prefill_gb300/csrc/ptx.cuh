@@ -335,6 +335,30 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 2^x for a pair of values on the FMA pipe, without MUFU (exp2_poly_fit.py
+// next to this file derives the method and the coefficients):
+//   clamp x >= -127; n = round(x) by adding 1.5 * 2^23 (the sum's low
+//   mantissa bits then hold n); f = x - n in [-1/2, 1/2];
+//   2^f ~ 1 + f (c1 + f (c2 + f c3)), a minimax fit of the relative error
+//   with p(0) = 1 exactly (max relative error 1.02e-4, far below the bf16
+//   rounding that P gets next); 2^n is added to the exponent field.
+// For x below -126 the result is a tiny or zero value, like ex2.approx.ftz.
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  constexpr float c1 = 0x1.62f5fap-1f, c2 = 0x1.f00c4cp-3f, c3 = 0x1.c2a216p-5f;
+  x.x = fmaxf(x.x, -127.0f);
+  x.y = fmaxf(x.y, -127.0f);
+  const float2 t = __fadd2_rn(x, make_float2(kMagic, kMagic));
+  const float2 n = __fadd2_rn(t, make_float2(-kMagic, -kMagic));
+  const float2 f = __ffma2_rn(n, make_float2(-1.0f, -1.0f), x);
+  float2 p = __ffma2_rn(make_float2(c3, c3), f, make_float2(c2, c2));
+  p = __ffma2_rn(p, f, make_float2(c1, c1));
+  p = __ffma2_rn(p, f, make_float2(1.0f, 1.0f));
+  const uint32_t bx = __float_as_uint(p.x) + (__float_as_uint(t.x) << 23);
+  const uint32_t by = __float_as_uint(p.y) + (__float_as_uint(t.y) << 23);
+  return make_float2(__uint_as_float(bx), __uint_as_float(by));
+}
+
 // max of three (sm_100+ three-input form)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
