@@ -5,7 +5,7 @@ bit in the status word of the call's workspace, makes the CTA's other roles
 stop waiting, lets the copies and MMAs it already issued finish (again with a
 bound), frees TMEM and returns, so the context stays usable.  The product
 library waits 4 s.  This test loads a separate test build (build variant
-"waittest") that waits 50 ms and can withhold CTA 0's first K/V tile: that
+"testhooks") that waits 50 ms and can withhold CTA 0's first K/V tile: that
 tile is neither copied nor announced to its barrier, so the MMA warp's wait on
 it runs out while no copy is in flight on that slot.  Each workspace kind (the
 library's own, a caller's, the no-alloc scratch) must then report
@@ -27,7 +27,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(scope="module")
 def waitlib(cuda_lib):
     from variable_length_prefill_gb300 import _binding
-    lib = ctypes.CDLL(cuda_lib.build(variant="waittest"))
+    lib = ctypes.CDLL(cuda_lib.build(variant="testhooks"))
     for name, (res, args) in _binding.SYMBOLS.items():
         fn = getattr(lib, name)
         fn.restype = res
@@ -74,7 +74,7 @@ def test_wait_runs_out_and_is_reported(waitlib, kind):
     # a normal call first: module loaded, result right, status clear
     assert _run(waitlib, kind, t, cu_q, cu_k, out, s, ws) == 0
     assert _check(waitlib, kind, s, ws) == 0
-    assert_close(to_bits(out), ref, f"waittest build, {kind} workspace")
+    assert_close(to_bits(out), ref, f"testhooks build, {kind} workspace")
 
     waitlib.attn_varlen_test_withhold(1)
     try:
@@ -95,7 +95,7 @@ def test_wait_runs_out_and_is_reported(waitlib, kind):
     out.zero_()
     assert _run(waitlib, kind, t, cu_q, cu_k, out, s, ws) == 0
     assert _check(waitlib, kind, s, ws) == 0
-    assert_close(to_bits(out), ref, f"waittest build after a timeout, {kind} workspace")
+    assert_close(to_bits(out), ref, f"testhooks build after a timeout, {kind} workspace")
 
 
 def test_product_library_has_no_test_hook(cuda_lib):

@@ -19,11 +19,11 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libattn_varlen.so"
 # Test-only builds: the same sources with extra defines, in a library of their
-# own that the product never loads.  "waittest" shortens every kernel wait to
+# own that the product never loads.  "testhooks" shortens every kernel wait to
 # 50 ms and compiles the hook that withholds one K/V tile, so a test can run
 # a wait out and check the reported status.
 VARIANTS = {
-    "waittest": ("libattn_varlen_waittest.so",
+    "testhooks": ("libattn_varlen_testhooks.so",
                  ["-DATTN_VARLEN_WAIT_LIMIT_NS=50000000ull", "-DATTN_VARLEN_TEST_HOOKS=1"]),
 }
 SOURCES = ["attn_varlen_api.cu", "attn_varlen_kernels.cu", "paged_decode.cu", "chunk_o.cu"]

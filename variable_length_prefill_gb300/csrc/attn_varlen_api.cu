@@ -112,34 +112,39 @@ int check_args(const void* q, const void* k, const void* v, const int32_t* cu_q,
 namespace avp {
 
 int encode_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int num_heads, int head_dim,
-               uint64_t rows, int box_rows) {
-  const int box = box_cols(head_dim);
+               uint64_t rows, int box_rows, int box_cols, bool swizzle_128) {
   cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_heads * head_dim * 2};
-  cuuint32_t boxdim[3] = {(cuuint32_t)box, 1, (cuuint32_t)box_rows};
+  cuuint32_t boxdim[3] = {(cuuint32_t)box_cols, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapSwizzle swz =
-      box_swizzle_128(head_dim) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B;
+      swizzle_128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   return (int)enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                   boxdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-// Templates: a 3-D bf16 map {head_dim, num_heads, rows} with box {box, 1,
-// rows per tile} (128 query rows for q, kv_tile_rows keys for k and v); the
+// Templates: a 3-D bf16 map {head_dim, num_heads, rows} with box {cols, 1,
+// rows per tile} (128 query rows for q, kv_tile_rows keys for k and v), one
+// for box A (columns [0, 64)) and one for box B (the columns past 64); the
 // plan kernel patches the address and the row extent per sequence.
 // Class 0 is encoded one row short of kMapLargeBytes, class 1 at it.
-int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[kMapsPerSeq],
+int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[kTensors],
                      int num_heads, int head_dim) {
   const uint64_t row_bytes = (uint64_t)num_heads * head_dim * 2;
   const uint64_t large_rows = (kMapLargeBytes + row_bytes - 1) / row_bytes;
   const uint64_t small_rows = large_rows > 1 ? large_rows - 1 : 1;
   for (int m = 0; m < kMapsPerSeq; ++m) {
-    const int box_rows = m == 0 ? kBlockM : kv_tile_rows(head_dim);
-    int r = encode_map(enc, &pp.tmpl[0][m], bases[m], num_heads, head_dim, small_rows, box_rows);
-    if (r) return r;
-    r = encode_map(enc, &pp.tmpl[1][m], bases[m], num_heads, head_dim, large_rows, box_rows);
-    if (r) return r;
+    const int t = m % kTensors;
+    const bool b = m >= kTensors;
+    const int box_rows = t == 0 ? kBlockM : kv_tile_rows(head_dim);
+    const int cols = b ? box_b_cols(head_dim) : box_cols(head_dim);
+    const bool swz = b ? box_b_swizzle_128(head_dim) : true;
+    for (int cls = 0; cls < 2; ++cls) {
+      const int r = encode_map(enc, &pp.tmpl[cls][m], bases[t], num_heads, head_dim,
+                               cls ? large_rows : small_rows, box_rows, cols, swz);
+      if (r) return r;
+    }
   }
   return 0;
 }
@@ -155,11 +160,11 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const 
         DeviceState& st, cudaStream_t stream, bool causal = false) {
   avp::PlanParams pp;
   std::memset(&pp, 0, sizeof(pp));
-  const void* bases[avp::kMapsPerSeq] = {q, k, v};
+  const void* bases[avp::kTensors] = {q, k, v};
   if (avp::encode_templates(reinterpret_cast<avp::EncodeTiledFn>(g_encode), pp, bases, num_heads,
                             head_dim) != 0)
     return ATTN_VARLEN_ERR_DRIVER;
-  for (int m = 0; m < avp::kMapsPerSeq; ++m) pp.base[m] = static_cast<const uint8_t*>(bases[m]);
+  for (int m = 0; m < avp::kTensors; ++m) pp.base[m] = static_cast<const uint8_t*>(bases[m]);
   pp.cu_q = cu_q;
   pp.cu_k = cu_k;
   pp.ws = static_cast<uint8_t*>(ws);

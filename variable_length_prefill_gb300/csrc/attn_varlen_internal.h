@@ -14,7 +14,10 @@ namespace avp {
 // (128 for head_dim 128, 112 for head_dim 72).
 constexpr int kBlockM = 128;
 constexpr int kUnitRows = 2 * kBlockM;
-constexpr int kMapsPerSeq = 3;       // q, k, v tensor maps per sequence
+constexpr int kTensors = 3;          // q, k, v
+// Tensor maps per sequence: [0, 3) box A of q, k, v (64 columns, 128-byte
+// swizzle), [3, 6) box B of q, k, v (the columns past 64; see box_b_cols)
+constexpr int kMapsPerSeq = 2 * kTensors;
 constexpr int kMapBytes = 128;       // sizeof(CUtensorMap)
 constexpr int kLptMaxSeqs = 2048;    // longest-first ordering up to this many sequences
 
@@ -82,7 +85,7 @@ struct PlanParams {
   CUtensorMap tmpl[2][kMapsPerSeq];
   const int32_t* cu_q;
   const int32_t* cu_k;
-  const uint8_t* base[kMapsPerSeq];  // q, k, v
+  const uint8_t* base[kTensors];  // q, k, v
   uint8_t* ws;
   uint8_t* split;  // tail-split region, or null
   int split_cap;   // items the split region holds (0: no tail split)
@@ -99,13 +102,14 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Encode one [rows, num_heads, head_dim] bf16 map with this library's box
-// (box_cols(head_dim) x 1 x box_rows) and swizzle (attn_varlen_api.cu).
-// Returns the CUresult.
+// Encode one [rows, num_heads, head_dim] bf16 map with a box of box_cols x 1
+// x box_rows, 128-byte swizzled or not (attn_varlen_api.cu).  Returns the
+// CUresult.
 int encode_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int num_heads, int head_dim,
-               uint64_t rows, int box_rows);
-// Fill pp.tmpl for q, k, v at `bases` (both size classes).  Returns a CUresult.
-int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[kMapsPerSeq],
+               uint64_t rows, int box_rows, int box_cols, bool swizzle_128);
+// Fill pp.tmpl for q, k, v at `bases` (both size classes, both boxes).
+// Returns a CUresult.
+int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[kTensors],
                      int num_heads, int head_dim);
 
 struct FwdParams {
@@ -130,8 +134,9 @@ cudaError_t prepare_fwd(int head_dim);  // per device and head_dim, before the f
 cudaError_t launch_fwd(int head_dim, const FwdParams& p, int grid, cudaStream_t stream);
 int fwd_threads(int head_dim);
 size_t fwd_smem_bytes(int head_dim);
-int box_cols(int head_dim);      // TMA box width in columns for this head_dim
+int box_cols(int head_dim);      // width of TMA box A (64 columns, 128-byte swizzle)
+int box_b_cols(int head_dim);    // width of box B: columns [64, 64 + box_b_cols)
+bool box_b_swizzle_128(int head_dim);  // box B 128-byte swizzled (else unswizzled)
 int kv_tile_rows(int head_dim);  // keys per K/V tile (TMA box height of the k and v maps)
-bool box_swizzle_128(int head_dim);
 
 }  // namespace avp

@@ -104,10 +104,10 @@ constexpr uint64_t kWaitLimitNs = ATTN_VARLEN_WAIT_LIMIT_NS;
 constexpr int kMergeTiles = 8;
 
 
-// K/V ring depth per head_dim (shared memory: head_dim 72 holds 2 x 32 KB of
-// Q and 28 KB per stage, head_dim 128 2 x 32 KB and 32 KB per stage)
+// K/V ring depth per head_dim (shared memory: head_dim 72 holds 2 x 18 KB of
+// Q and 16 KB per stage, head_dim 128 2 x 32 KB and 32 KB per stage)
 #ifndef ATTN_VARLEN_KV_STAGES_72
-#define ATTN_VARLEN_KV_STAGES_72 4
+#define ATTN_VARLEN_KV_STAGES_72 8
 #endif
 #ifndef ATTN_VARLEN_KV_STAGES_128
 #define ATTN_VARLEN_KV_STAGES_128 4
@@ -115,11 +115,12 @@ constexpr int kMergeTiles = 8;
 
 // Share of the softmax's exponentials computed on the FMA pipe
 // (exp2_poly2) instead of the MUFU unit: POLY of every 7 groups of four
-// columns.  The MUFU unit retires 16 exponentials per clock per SM and
-// bounds the softmax of the small head dims; moving about 3/7 of them to
-// FMA arithmetic (about five issue slots each) balances the two.
+// columns.  Off by default: on GB300 the MUFU unit retires ex2 fast enough
+// that the softmax is bound by issue slots, and each polynomial costs about
+// six instructions against one; 2/7, 3/7 and 4/7 made the head_dim-72
+// kernel 13, 21 and 35 % slower.
 #ifndef ATTN_VARLEN_POLY_SMALL
-#define ATTN_VARLEN_POLY_SMALL 3
+#define ATTN_VARLEN_POLY_SMALL 0
 #endif
 #ifndef ATTN_VARLEN_POLY_128
 #define ATTN_VARLEN_POLY_128 0
@@ -136,6 +137,7 @@ template <>
 struct Cfg<64> {
   static constexpr int DP = 64;
   static constexpr int BW = 64;    // one 64-column box
+  static constexpr int WB = 0;    // one box
   static constexpr int KN = 128;
   static constexpr bool PSEP = true;
   static constexpr int ISSUERS = 2;
@@ -147,6 +149,7 @@ template <>
 struct Cfg<80> {
   static constexpr int DP = 80;
   static constexpr int BW = 64;    // second box: columns 64-79 and zero fill
+  static constexpr int WB = 64;   // box B: columns 64-127, 128-byte swizzle
   static constexpr int KN = 112;
   static constexpr bool PSEP = true;
   static constexpr int ISSUERS = 2;
@@ -158,6 +161,7 @@ template <>
 struct Cfg<96> {
   static constexpr int DP = 96;
   static constexpr int BW = 64;    // second box: columns 64-95 and zero fill
+  static constexpr int WB = 64;   // box B: columns 64-127, 128-byte swizzle
   static constexpr int KN = 96;
   static constexpr bool PSEP = true;
   static constexpr int ISSUERS = 2;
@@ -168,8 +172,9 @@ struct Cfg<96> {
 template <>
 struct Cfg<72> {
   static constexpr int DP = 80;    // padded head_dim (MMA K and N multiple of 16)
-  static constexpr int BW = 64;    // columns per TMA box: two boxes, the second
-                                   // holding columns 64-71 and zero fill
+  static constexpr int BW = 64;    // box A: columns 0-63, 128-byte swizzle
+  static constexpr int WB = 8;     // box B: columns 64-71, unswizzled; the MMAs take
+                                   // columns 72-79 from a zero region in shared memory
   static constexpr int KN = 112;   // keys per K/V tile
   static constexpr bool PSEP = true;  // P in TMEM columns of its own
   static constexpr int ISSUERS = 2;   // one MMA-issuing warp per Q tile
@@ -181,6 +186,7 @@ template <>
 struct Cfg<128> {
   static constexpr int DP = 128;
   static constexpr int BW = 64;
+  static constexpr int WB = 64;   // box B: columns 64-127, 128-byte swizzle
   static constexpr int KN = 128;
   static constexpr bool PSEP = false;  // P overwrites the first half of S
   static constexpr int ISSUERS = 1;    // one MMA-issuing warp for both Q tiles
@@ -203,15 +209,30 @@ struct Geometry {
   static constexpr uint32_t SWZ = Cfg<D>::SWZ;
   static constexpr int POLY = Cfg<D>::POLY;
   static_assert(POLY >= 0 && POLY <= kPolyDen, "polynomial share");
-  static constexpr uint32_t Q_BOX_BYTES = kBlockM * BW * 2;  // one box: 128 rows x BW
-  static constexpr uint32_t Q_TILE_BYTES = NB * Q_BOX_BYTES;
-  static constexpr uint32_t KV_BOX_BYTES = KN * BW * 2;      // one box: KN keys x BW
-  static constexpr uint32_t KV_TILE_BYTES = NB * KV_BOX_BYTES;
+  // Box B (columns 64 and up) is either a second 64-column, 128-byte
+  // swizzled box (ZB false) or, for head_dim 72, an unswizzled 8-column box
+  // (ZB true) whose 16-byte rows form the core matrices of the MMAs' last
+  // 16-column step together with a 16-byte-wide zero region (ZERO_OFF):
+  // every copied byte is a real input byte, and no TMA zero fill is used.
+  static constexpr int WB = Cfg<D>::WB;
+  static constexpr bool ZB = WB == 8;
+  static_assert(NB == 1 ? WB == 0 : (WB == BW || (ZB && DP == BW + 16)), "box B");
+  static constexpr uint32_t Q_BOX_BYTES = kBlockM * BW * 2;  // box A: 128 rows x BW
+  static constexpr uint32_t Q_BOXB_BYTES = NB == 1 ? 0u : kBlockM * WB * 2;
+  static constexpr uint32_t Q_LOAD_BYTES = Q_BOX_BYTES + Q_BOXB_BYTES;  // bytes one Q tile copies
+  static constexpr uint32_t Q_TILE_BYTES = (Q_LOAD_BYTES + 1023u) / 1024u * 1024u;
+  static constexpr uint32_t KV_BOX_BYTES = KN * BW * 2;      // box A: KN keys x BW
+  static constexpr uint32_t KV_BOXB_BYTES = NB == 1 ? 0u : KN * WB * 2;
+  static constexpr uint32_t KV_LOAD_BYTES = KV_BOX_BYTES + KV_BOXB_BYTES;
+  static constexpr uint32_t KV_TILE_BYTES = (KV_LOAD_BYTES + 1023u) / 1024u * 1024u;
   static_assert(KV_BOX_BYTES % 1024 == 0, "128B-swizzled boxes start on 1024-byte boundaries");
   static constexpr uint32_t SBO = 8 * BW * 2;               // 8-row group stride
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t KV_OFF = 2 * Q_TILE_BYTES;
-  static constexpr uint32_t BAR_OFF = KV_OFF + STAGES * KV_TILE_BYTES;
+  // zero region: 128 rows x 16 bytes (ZB only)
+  static constexpr uint32_t ZERO_OFF = KV_OFF + STAGES * KV_TILE_BYTES;
+  static constexpr uint32_t ZERO_BYTES = ZB ? kBlockM * 16u : 0u;
+  static constexpr uint32_t BAR_OFF = ZERO_OFF + ZERO_BYTES;
   // barrier slots (8 bytes each)
   static constexpr int B_Q_FULL = 0, B_Q_EMPTY = 1, B_KV_FULL = 2, B_KV_EMPTY = 2 + STAGES,
                        B_S_FULL = 2 + 2 * STAGES, B_P_FULL = B_S_FULL + 2,
@@ -408,28 +429,31 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
 
   // 1. per sequence: lengths, sort key, tensor maps
   bool wrote_map = false;
-  for (int i = tid; i < N; i += nt) {
-    const int q0 = p.cu_q[i], lq = p.cu_q[i + 1] - q0;
-    const int k0 = p.cu_k[i], lk = p.cu_k[i + 1] - k0;
-    const bool live = lq > 0;
-    if (lpt) {
+  if (lpt) {
+    for (int i = tid; i < N; i += nt) {
+      const int lq = p.cu_q[i + 1] - p.cu_q[i];
+      const int lk = p.cu_k[i + 1] - p.cu_k[i];
       s_lq[i] = lq;
       s_lk[i] = lk;
-      s_key[i] = live ? (lk > 0 ? lk : 0) : -1;
+      s_key[i] = lq > 0 ? (lk > 0 ? lk : 0) : -1;
     }
-    if (live && lk > 0) {
-      for (int m = 0; m < kMapsPerSeq; ++m) {
-        uint8_t* dst = p.ws + L.maps + ((size_t)i * kMapsPerSeq + m) * kMapBytes;
-        const int row0 = (m == 0) ? q0 : k0;
-        const int len = (m == 0) ? lq : lk;
-        const int cls = (uint64_t)len * (uint64_t)p.row_bytes >= kMapLargeBytes ? 1 : 0;
-        const uint4* src = reinterpret_cast<const uint4*>(&p.tmpl[cls][m]);
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
+  }
+  // one thread per (sequence, map): the q, k and v maps of box A and box B
+  for (int idx = tid; idx < N * kMapsPerSeq; idx += nt) {
+    const int i = idx / kMapsPerSeq, m = idx - i * kMapsPerSeq, t = m % kTensors;
+    const int q0 = p.cu_q[i], lq = p.cu_q[i + 1] - q0;
+    const int k0 = p.cu_k[i], lk = p.cu_k[i + 1] - k0;
+    if (lq > 0 && lk > 0) {
+      uint8_t* dst = p.ws + L.maps + (size_t)idx * kMapBytes;
+      const int row0 = t == 0 ? q0 : k0;
+      const int len = t == 0 ? lq : lk;
+      const int cls = (uint64_t)len * (uint64_t)p.row_bytes >= kMapLargeBytes ? 1 : 0;
+      const uint4* src = reinterpret_cast<const uint4*>(&p.tmpl[cls][m]);
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-        for (int w = 0; w < kMapBytes / 16; ++w) d4[w] = src[w];
-        tmap_set_address(dst, p.base[m] + (size_t)row0 * p.row_bytes);
-        tmap_set_dim2(dst, (uint32_t)len);
-      }
+      for (int w = 0; w < kMapBytes / 16; ++w) d4[w] = src[w];
+      tmap_set_address(dst, p.base[t] + (size_t)row0 * p.row_bytes);
+      tmap_set_dim2(dst, (uint32_t)len);
       wrote_map = true;
     }
   }
@@ -714,6 +738,12 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
     tmem_alloc(base + G::MISC_OFF, kTmemCols);
     tmem_relinquish();
   }
+  if constexpr (G::ZB) {
+    // the zero region, read by the MMAs (async proxy) from now on
+    if (threadIdx.x < G::ZERO_BYTES / 16u)
+      reinterpret_cast<uint4*>(base_ptr + G::ZERO_OFF)[threadIdx.x] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -762,27 +792,35 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       const UnitInfo ui = decode_item(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, G::KN,
                                         split_start, num_units, tail_prefix, p.causal != 0);
       if (ui.nkv == 0) continue;
+      // maps of this sequence: box A of q, k, v, then box B of q, k, v
       const uint8_t* mq = p.ws + L.maps + (size_t)ui.seq * kMapsPerSeq * kMapBytes;
       const uint8_t* mk = mq + kMapBytes;
       const uint8_t* mv = mq + 2 * kMapBytes;
+      const uint8_t* mqb = G::ZB ? mq + kTensors * kMapBytes : mq;
+      const uint8_t* mkb = G::ZB ? mk + kTensors * kMapBytes : mk;
+      const uint8_t* mvb = G::ZB ? mv + kTensors * kMapBytes : mv;
       if (leader) {
         tmap_acquire(mq);
         tmap_acquire(mk);
         tmap_acquire(mv);
+        if (G::ZB) {
+          tmap_acquire(mqb);
+          tmap_acquire(mkb);
+          tmap_acquire(mvb);
+        }
       }
       __syncwarp();
       if (!(ok = wait_(bar(G::B_Q_EMPTY), (q_use & 1u) ^ 1u))) break;
       ++q_use;
-      mbar_arrive_expect_tx_if(leader, bar(G::B_Q_FULL), (ui.t1 ? 2u : 1u) * G::Q_TILE_BYTES);
-#pragma unroll
-      for (int b = 0; b < G::NB; ++b)
-        tma_load_3d_if(leader, sQ + b * G::Q_BOX_BYTES, mq, bar(G::B_Q_FULL), b * G::BW, ui.head,
-                       ui.q0);
-      if (ui.t1) {
-#pragma unroll
-        for (int b = 0; b < G::NB; ++b)
-          tma_load_3d_if(leader, sQ + G::Q_TILE_BYTES + b * G::Q_BOX_BYTES, mq, bar(G::B_Q_FULL),
-                         b * G::BW, ui.head, ui.q0 + kBlockM);
+      mbar_arrive_expect_tx_if(leader, bar(G::B_Q_FULL), (ui.t1 ? 2u : 1u) * G::Q_LOAD_BYTES);
+      // box A at x = 0; box B at x = 64, right after box A (the whole tile
+      // for ZB, the second 64-column box otherwise)
+      for (int t = 0; t < (ui.t1 ? 2 : 1); ++t) {
+        const uint32_t dq = sQ + t * G::Q_TILE_BYTES;
+        tma_load_3d_if(leader, dq, mq, bar(G::B_Q_FULL), 0, ui.head, ui.q0 + t * kBlockM);
+        if (G::NB == 2)
+          tma_load_3d_if(leader, dq + G::Q_BOX_BYTES, mqb, bar(G::B_Q_FULL), G::BW, ui.head,
+                         ui.q0 + t * kBlockM);
       }
       for (int i = 0; i < 2 * ui.nkv; ++i) {
         int j;
@@ -795,13 +833,13 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
 #else
         const uint32_t issue = leader;
 #endif
-        mbar_arrive_expect_tx_if(issue, bar(G::B_KV_FULL + stage), G::KV_TILE_BYTES);
-        const uint8_t* m = is_v ? mv : mk;
+        mbar_arrive_expect_tx_if(issue, bar(G::B_KV_FULL + stage), G::KV_LOAD_BYTES);
         const uint32_t dst = sKV + stage * G::KV_TILE_BYTES;
-#pragma unroll
-        for (int b = 0; b < G::NB; ++b)
-          tma_load_3d_if(issue, dst + b * G::KV_BOX_BYTES, m, bar(G::B_KV_FULL + stage),
-                         b * G::BW, ui.head, (ui.jb + j) * G::KN);
+        const int row = (ui.jb + j) * G::KN;
+        tma_load_3d_if(issue, dst, is_v ? mv : mk, bar(G::B_KV_FULL + stage), 0, ui.head, row);
+        if (G::NB == 2)
+          tma_load_3d_if(issue, dst + G::KV_BOX_BYTES, is_v ? mvb : mkb, bar(G::B_KV_FULL + stage),
+                         G::BW, ui.head, row);
         ++kv_item;
       }
     }
@@ -840,6 +878,13 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       return __all_sync(0xffffffffu,
                         wait_bounded(b, parity, abort_flag, p.status, kStatusTimeoutMma));
     };
+    // Box B with a zero chunk (ZB): unswizzled core matrices of 8 rows x 16
+    // bytes.  K-major (Q, K): the K-direction step to the second 8-column
+    // chunk (LBO) lands in the zero region, 8-row groups are 128 bytes apart
+    // (SBO).  MN-major (V): 8-key groups 128 bytes apart (LBO), the second
+    // 8-column chunk of N (SBO) in the zero region.
+    const uint32_t sZero = base + G::ZERO_OFF;
+    auto desc_kb = [&](uint32_t addr) { return smem_desc(addr, sZero - addr, 128, kSwizzleNone); };
     // S_t = Q_t K^T : K from stage `ks`
     auto issue_s = [&](int t, uint32_t ks) {
       const uint64_t qa = dq0 + ((t * G::Q_TILE_BYTES) >> 4);
@@ -849,19 +894,39 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       for (int k = 0; k < G::NK_S; ++k) {
         const uint32_t box = (uint32_t)(k * 16 / G::BW);
         const uint32_t col_b = (uint32_t)((k * 16) % G::BW) * 2;
-        mma_ss_if(leader, d, qa + ((box * G::Q_BOX_BYTES + col_b) >> 4),
-                  kb + ((box * G::KV_BOX_BYTES + col_b) >> 4), idesc_s, k > 0 ? 1u : 0u);
+        if (G::ZB && box == 1) {
+          mma_ss_if(leader, d, desc_kb(sQ + t * G::Q_TILE_BYTES + G::Q_BOX_BYTES),
+                    desc_kb(sKV + ks * G::KV_TILE_BYTES + G::KV_BOX_BYTES), idesc_s, 1u);
+        } else {
+          mma_ss_if(leader, d, qa + ((box * G::Q_BOX_BYTES + col_b) >> 4),
+                    kb + ((box * G::KV_BOX_BYTES + col_b) >> 4), idesc_s, k > 0 ? 1u : 0u);
+        }
       }
     };
-    // O_t (+)= P_t V : V from stage `vs`, P from TMEM
+    // O_t (+)= P_t V : V from stage `vs`, P from TMEM.  With ZB, columns
+    // 0-63 (box A) and 64-79 (box B and the zero chunk) are two products of
+    // N = 64 and N = 16 per 16-key step.
+    constexpr uint32_t idesc_pv_a = idesc_bf16_f32(kBlockM, G::BW, false, true);
+    constexpr uint32_t idesc_pv_b = idesc_bf16_f32(kBlockM, 16, false, true);
     auto issue_pv = [&](int t, uint32_t vs, bool acc) {
       const uint64_t vb = dv0 + ((vs * G::KV_TILE_BYTES) >> 4);
       const uint32_t d = tmem + G::o_col(t);
       const uint32_t a = tmem + G::p_col(t);
+      if constexpr (G::ZB) {
+        const uint32_t vbb = sKV + vs * G::KV_TILE_BYTES + G::KV_BOX_BYTES;
+        const uint64_t dvb = smem_desc(vbb, 128, sZero - vbb, kSwizzleNone);
 #pragma unroll
-      for (int k = 0; k < G::NK_PV; ++k)
-        mma_ts_if(leader, d, a + 8u * k, vb + ((k * 16 * G::BW * 2) >> 4), idesc_pv,
-                  (acc || k > 0) ? 1u : 0u);
+        for (int k = 0; k < G::NK_PV; ++k) {
+          const uint32_t acc_k = (acc || k > 0) ? 1u : 0u;
+          mma_ts_if(leader, d, a + 8u * k, vb + ((k * 16 * G::BW * 2) >> 4), idesc_pv_a, acc_k);
+          mma_ts_if(leader, d + G::BW, a + 8u * k, dvb + ((k * 16 * 16) >> 4), idesc_pv_b, acc_k);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < G::NK_PV; ++k)
+          mma_ts_if(leader, d, a + 8u * k, vb + ((k * 16 * G::BW * 2) >> 4), idesc_pv,
+                    (acc || k > 0) ? 1u : 0u);
+      }
     };
     // S_t overwrites P_t: the P.V MMA that reads P_t must be finished
     // (issue order guarantees it unless kStrictPvWait asks for the wait)
@@ -1303,9 +1368,15 @@ int kv_tile_rows(int head_dim) {
   return with_head_dim(head_dim, [](auto d) { return Cfg<decltype(d)::value>::KN; });
 }
 
-bool box_swizzle_128(int head_dim) {
-  return with_head_dim(head_dim,
-                       [](auto d) { return Cfg<decltype(d)::value>::SWZ == kSwizzle128B; });
+int box_b_cols(int head_dim) {
+  return with_head_dim(head_dim, [](auto d) {
+    using G = Geometry<decltype(d)::value>;
+    return G::NB == 1 ? G::BW : G::WB;  // one box: box B is never loaded
+  });
+}
+
+bool box_b_swizzle_128(int head_dim) {
+  return with_head_dim(head_dim, [](auto d) { return !Geometry<decltype(d)::value>::ZB; });
 }
 
 }  // namespace avp

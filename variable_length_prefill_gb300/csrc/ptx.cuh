@@ -318,6 +318,12 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
   return old;
 }
 
+// Make this thread's generic-proxy writes to shared memory visible to the
+// async proxy (TMA, tcgen05.mma operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Programmatic dependent launch: the running grid lets the next grid on the
 // stream start launching; the dependent grid waits for this grid to finish
 // and its memory to be visible before it reads what this grid wrote.
