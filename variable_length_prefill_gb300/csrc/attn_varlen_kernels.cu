@@ -70,8 +70,6 @@ namespace avp {
 
 namespace {
 
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;  // first MMA-issuing warp (and TMEM owner)
 constexpr int kItemDepth = 4; // work items handed from the producer to the other roles
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
@@ -106,6 +104,20 @@ constexpr int kMergeTiles = 8;
 
 // K/V ring depth per head_dim (shared memory: head_dim 72 holds 2 x 18 KB of
 // Q and 16 KB per stage, head_dim 128 2 x 32 KB and 32 KB per stage)
+#ifndef ATTN_VARLEN_HALVES
+#define ATTN_VARLEN_HALVES 1
+#endif
+// head_dim 72: the row sum of P comes out of the P.V product as O column 72
+// (V's padding column 72 reads 1.0 from a "ones" region), instead of being
+// added up by the softmax threads.
+// Store P in chunks of 8 packed columns as they are computed (always with
+// HALVES = 2; optional with one thread per row).
+#ifndef ATTN_VARLEN_P_CHUNKS
+#define ATTN_VARLEN_P_CHUNKS 0
+#endif
+#ifndef ATTN_VARLEN_SUM_IN_O
+#define ATTN_VARLEN_SUM_IN_O 1
+#endif
 #ifndef ATTN_VARLEN_KV_STAGES_72
 #define ATTN_VARLEN_KV_STAGES_72 8
 #endif
@@ -203,7 +215,16 @@ struct Geometry {
   static constexpr bool PSEP = Cfg<D>::PSEP;
   static constexpr int ISSUERS = Cfg<D>::ISSUERS;
   static_assert(PSEP || ISSUERS == 1, "two issuers need P in columns of its own");
-  static constexpr int THREADS = 32 * (kMmaWarp + ISSUERS);
+  // Softmax threads per Q-tile row: with HALVES = 2 two threads share each
+  // row, one per half of the key tile's columns (four softmax warps per SM
+  // sub-partition instead of two, to hide the latency of each row's chain).
+  static constexpr int HALVES = PSEP ? ATTN_VARLEN_HALVES : 1;
+  static_assert(HALVES == 1 || HALVES == 2, "halves");
+  static constexpr int KC = KN / HALVES;                  // key columns per softmax thread
+  static constexpr int SM_WARPS = 8 * HALVES;             // softmax warps: 2 tiles x HALVES x 4
+  static constexpr int LOAD_WARP = SM_WARPS;              // TMA producer
+  static constexpr int MMA_WARP = SM_WARPS + 1;           // first MMA issuer (and TMEM owner)
+  static constexpr int THREADS = 32 * (MMA_WARP + ISSUERS);
   static constexpr int NB = (DP + BW - 1) / BW;             // boxes per tile
   static constexpr int STAGES = Cfg<D>::STAGES;
   static constexpr uint32_t SWZ = Cfg<D>::SWZ;
@@ -232,18 +253,29 @@ struct Geometry {
   // zero region: 128 rows x 16 bytes (ZB only)
   static constexpr uint32_t ZERO_OFF = KV_OFF + STAGES * KV_TILE_BYTES;
   static constexpr uint32_t ZERO_BYTES = ZB ? kBlockM * 16u : 0u;
-  static constexpr uint32_t BAR_OFF = ZERO_OFF + ZERO_BYTES;
+  // LO: O column D (= 72) accumulates sum_k P[r, k], the row sum, because
+  // V's padding column 72 reads 1.0 from the ones region (128 rows x 16 B,
+  // each row 1.0 then seven zeros) instead of the zero region.
+  static constexpr bool LO = ZB && ATTN_VARLEN_SUM_IN_O != 0;
+  static constexpr uint32_t ONES_OFF = ZERO_OFF + ZERO_BYTES;
+  static constexpr uint32_t ONES_BYTES = LO ? kBlockM * 16u : 0u;
+  // row-statistics exchange between the two threads of a row (HALVES = 2):
+  // float [2 buffers][2 tiles][2 halves][128 rows]
+  static constexpr uint32_t XCH_OFF = ONES_OFF + ONES_BYTES;
+  static constexpr uint32_t XCH_BYTES = HALVES == 2 ? 2u * 2u * 2u * kBlockM * 4u : 0u;
+  static constexpr uint32_t BAR_OFF = XCH_OFF + XCH_BYTES;
   // barrier slots (8 bytes each)
   static constexpr int B_Q_FULL = 0, B_Q_EMPTY = 1, B_KV_FULL = 2, B_KV_EMPTY = 2 + STAGES,
                        B_S_FULL = 2 + 2 * STAGES, B_P_FULL = B_S_FULL + 2,
                        B_PV_DONE = B_P_FULL + 2, B_S_FREE = B_PV_DONE + 2,
                        B_DRAIN = B_S_FREE + 2, B_ITEM_FULL = B_DRAIN + 2,
                        B_ITEM_EMPTY = B_ITEM_FULL + kItemDepth,
-                       NUM_BARS = B_ITEM_EMPTY + kItemDepth;
+                       B_XCH = B_ITEM_EMPTY + kItemDepth,  // per (tile, lane quarter)
+                       NUM_BARS = B_XCH + (HALVES == 2 ? 8 : 0);
   // tmem slot, abort flag, then the item ring (kItemDepth int32)
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = MISC_OFF + 8 + 4 * kItemDepth + 1024;  // + alignment slack
-  static constexpr int ITEM_CONSUMERS = 8 + ISSUERS;  // warps that read each ring entry
+  static constexpr int ITEM_CONSUMERS = SM_WARPS + ISSUERS;  // warps that read each ring entry
   static_assert(SMEM_BYTES <= 232448, "shared memory above the sm_103 per-block limit");
   static constexpr int NK_S = DP / 16;  // K-steps of S = Q K^T
   static constexpr int NK_PV = KN / 16; // K-steps of O += P V
@@ -594,25 +626,30 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
   }
 }
 
-// Epilogue of one chunk of a split unit for one row (softmax warpgroup t,
-// row r): the unnormalised O row and its (m, l) go to partial slot `part`;
-// the last chunk of the unit to finish that row (a counter per row and Q
-// tile) merges the unit's chunks in chunk order,
+// Epilogue of one chunk of a split unit for one row (softmax threads of Q
+// tile t, row r, column half h), in two steps.  split_store: the
+// unnormalised O row goes to partial slot `part`, each half writing its
+// 16-column chunks.  Then (in the caller) the halves combine their row sums,
+// which also orders the other half's stores before half 0's count, and
+// split_finish (half 0) writes (m, l) and counts the chunk in; the last chunk
+// of the unit to finish that row (a counter per row and Q tile) merges the
+// unit's chunks in chunk order,
 //   m* = max_c m_c,  O = sum_c 2^(m_c - m*) O_c,  l = sum_c 2^(m_c - m*) l_c,
-// and writes O / l as bf16.  Each thread works alone (no barrier).  A slot
-// is column-major ([column][128 rows]) so that a warp's stores and loads of
-// one column are one 128-byte line; partials bypass L1, and the counter's
+// and writes O / l as bf16.  No thread waits for another CTA.  A slot is
+// column-major ([column][128 rows]) so that a warp's stores and loads of one
+// column are one 128-byte line; partials bypass L1, and the counter's
 // acquire-release add orders them between the chunks.
+constexpr size_t kSlot = (size_t)kPartRowMax * kBlockM;  // floats per (chunk, tile) slot
+
 template <int D>
-__device__ __noinline__ void split_epilogue(uint8_t* parts_base, int* counters, uint32_t tO, int t,
-                                            int r, float m, float l, uint16_t* orow, bool valid,
-                                            int part, int part0, int tail, int chunks) {
+__device__ __noinline__ void split_store(uint8_t* parts_base, uint32_t tO, int t, int r, int h,
+                                         int part) {
   using G = Geometry<D>;
-  constexpr size_t kSlot = (size_t)kPartRowMax * kBlockM;  // floats per (chunk, tile) slot
-  float* parts = reinterpret_cast<float*>(parts_base);
-  float* mine = parts + (size_t)(part * 2 + t) * kSlot + r;
+  constexpr int H = G::HALVES;
+  float* mine = reinterpret_cast<float*>(parts_base) + (size_t)(part * 2 + t) * kSlot + r;
 #pragma unroll
   for (int c = 0; c < G::DP; c += 16) {
+    if ((c / 16) % H != h) continue;
     uint32_t o[16];
     tmem_ld16(tO + c, o);
     tmem_wait_ld();
@@ -623,6 +660,15 @@ __device__ __noinline__ void split_epilogue(uint8_t* parts_base, int* counters, 
         if (c + e < D) __stcg(mine + (size_t)(c + e) * kBlockM, __uint_as_float(o[e]));
     }
   }
+}
+
+template <int D>
+__device__ __noinline__ void split_finish(uint8_t* parts_base, int* counters, int t, int r,
+                                          float m, float l, uint16_t* orow, bool valid, int part,
+                                          int part0, int tail, int chunks) {
+  using G = Geometry<D>;
+  float* parts = reinterpret_cast<float*>(parts_base);
+  float* mine = parts + (size_t)(part * 2 + t) * kSlot + r;
   __stcg(mine + (size_t)G::DP * kBlockM, m);
   __stcg(mine + (size_t)(G::DP + 1) * kBlockM, l);
   int* cnt = counters + ((size_t)(2 * tail + t) * kBlockM + r);
@@ -721,9 +767,9 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(G::B_S_FULL + t), 1);
-      mbar_init(bar(G::B_P_FULL + t), kBlockM);
+      mbar_init(bar(G::B_P_FULL + t), kBlockM * G::HALVES);
       mbar_init(bar(G::B_PV_DONE + t), 1);
-      mbar_init(bar(G::B_S_FREE + t), kBlockM);
+      mbar_init(bar(G::B_S_FREE + t), kBlockM * G::HALVES);
     }
     mbar_init(bar(G::B_DRAIN + 0), 1);
     mbar_init(bar(G::B_DRAIN + 1), 1);
@@ -731,17 +777,21 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       mbar_init(bar(G::B_ITEM_FULL + i), 1);
       mbar_init(bar(G::B_ITEM_EMPTY + i), G::ITEM_CONSUMERS);
     }
+    if (G::HALVES == 2)
+      for (int i = 0; i < 8; ++i) mbar_init(bar(G::B_XCH + i), 64);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == G::MMA_WARP) {
     tmem_alloc(base + G::MISC_OFF, kTmemCols);
     tmem_relinquish();
   }
   if constexpr (G::ZB) {
-    // the zero region, read by the MMAs (async proxy) from now on
+    // the zero (and ones) regions, read by the MMAs (async proxy) from now on
     if (threadIdx.x < G::ZERO_BYTES / 16u)
       reinterpret_cast<uint4*>(base_ptr + G::ZERO_OFF)[threadIdx.x] = make_uint4(0, 0, 0, 0);
+    if (G::LO && threadIdx.x < G::ONES_BYTES / 16u)  // bf16 1.0 in column 0 of each row
+      reinterpret_cast<uint4*>(base_ptr + G::ONES_OFF)[threadIdx.x] = make_uint4(0x3F80u, 0, 0, 0);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -760,7 +810,7 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
   const int32_t* order = reinterpret_cast<const int32_t*>(p.ws + L.order);
   const int32_t* prefix = reinterpret_cast<const int32_t*>(p.ws + L.prefix);
 
-  if (warp == kLoadWarp) {
+  if (warp == G::LOAD_WARP) {
     // ------------------------------------------------------ TMA producer
     // The whole warp runs the loop (uniform control flow); one elected lane
     // issues each TMA and expect-tx.  K and V tiles enter the ring in the
@@ -850,15 +900,15 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       for (uint32_t it = first; it < kv_item; ++it)
         wait_drain(bar(G::B_KV_FULL + it % G::STAGES), (it / G::STAGES) & 1u);
     }
-  } else if (warp >= kMmaWarp) {
+  } else if (warp >= G::MMA_WARP) {
     // ------------------------------------------------------- MMA issuer
     // The whole warp runs the loop; descriptors are computed once per tile
     // base and advanced by constants, and one elected lane issues each
     // tcgen05.mma and commit (commits track that lane's MMAs).  With two
-    // issuers, warp kMmaWarp + t issues every MMA of Q tile t, so neither
+    // issuers, warp MMA_WARP + t issues every MMA of Q tile t, so neither
     // tile's S waits behind the other tile's P.V in one in-order program;
     // K/V slots and the Q buffer are released by both.
-    const int mi = warp - kMmaWarp;
+    const int mi = warp - G::MMA_WARP;
     const uint32_t leader = elect_one();
     constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, G::KN, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, G::DP, false, true);
@@ -914,7 +964,8 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       const uint32_t a = tmem + G::p_col(t);
       if constexpr (G::ZB) {
         const uint32_t vbb = sKV + vs * G::KV_TILE_BYTES + G::KV_BOX_BYTES;
-        const uint64_t dvb = smem_desc(vbb, 128, sZero - vbb, kSwizzleNone);
+        const uint32_t pad = G::LO ? base + G::ONES_OFF : sZero;  // V columns 72-79
+        const uint64_t dvb = smem_desc(vbb, 128, pad - vbb, kSwizzleNone);
 #pragma unroll
         for (int k = 0; k < G::NK_PV; ++k) {
           const uint32_t acc_k = (acc || k > 0) ? 1u : 0u;
@@ -1078,21 +1129,45 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
     }
   } else {
     // --------------------------------------------------------- softmax
-    constexpr int KN = G::KN;
-    const int t = warp >> 2;                       // Q tile of this warpgroup
-    const int r = threadIdx.x & 127;               // row in the tile = TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_off + G::s_col(t);
-    const uint32_t tP = tmem + lane_off + G::p_col(t);
+    // Warp w: Q tile t = w / (4 H), column half h = (w / 4) mod H, TMEM lane
+    // quarter w mod 4.  Each thread owns row r of its tile (TMEM lane r) and
+    // the KC = KN / H key columns [h KC, (h + 1) KC) of every key tile.  With
+    // H = 2 the two threads of a row combine their partial row maxima every
+    // key tile, and their partial row sums once per unit, through shared
+    // memory and one mbarrier per (tile, lane quarter), whose waits are
+    // bounded like every other wait.  Output columns are handed out in
+    // 16-column chunks: chunk c / 16 belongs to half (c / 16) mod H.
+    constexpr int KN = G::KN, H = G::HALVES, KC = G::KC;
+    const int t = warp / (4 * H);                  // Q tile of this warp
+    const int h = (warp >> 2) % H;                 // column half
+    const int qq = warp & 3;                       // TMEM lane quarter
+    const int r = (qq << 5) | (threadIdx.x & 31);  // row in the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + G::s_col(t) + (uint32_t)(h * KC);
+    const uint32_t tP = tmem + lane_off + G::p_col(t) + (uint32_t)(h * KC / 2);
     const uint32_t tO = tmem + lane_off + G::o_col(t);
     const float sl2 = p.scale_log2;
-    uint32_t s_wait = 0, p_cnt = 0;
+    uint32_t s_wait = 0, p_cnt = 0, x_use = 0;
     bool ok = true;
 
     auto wait_ = [&](uint32_t b, uint32_t parity) -> bool {
       bool w = wait_bounded(b, parity, abort_flag, p.status, kStatusTimeoutSoftmax);
       return __all_sync(0xffffffffu, w);
     };
+    // H = 2: hand v to the other thread of this row and return its value.
+    // Two buffers alternate; a buffer is rewritten two exchanges later, after
+    // the partner has passed the next exchange and so finished reading it.
+    float* xch = reinterpret_cast<float*>(base_ptr + G::XCH_OFF);
+    const uint32_t xbar = bar(G::B_XCH + 4 * t + qq);
+    auto exchange = [&](float v, bool& okx) -> float {
+      float* slot = xch + (size_t)(((x_use & 1u) * 2u + (uint32_t)t) * H) * kBlockM;
+      slot[h * kBlockM + r] = v;
+      mbar_arrive(xbar);  // release: the store is visible to whoever sees the phase
+      okx = wait_(xbar, x_use & 1u);
+      ++x_use;
+      return slot[(1 - h) * kBlockM + r];
+    };
+    auto mine = [&](int c) { return (c / 16) % H == h; };  // 16-column output chunk
 
     for (int k = 0; ok; ++k) {
       const int u = next_item(k);
@@ -1109,9 +1184,9 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       const int klim = p.causal ? min(ui.lk, row + 1 + ui.coff) : ui.lk;
       if (nsteps == 0) {
         if (valid) {
-          uint4* o4 = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-          for (int c = 0; c < D * 2 / 16; ++c) o4[c] = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < D; c += 8)
+            if (mine(c)) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -1120,64 +1195,68 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
         if (!(ok = wait_(bar(G::B_S_FULL + t), s_wait & 1u))) break;
         ++s_wait;
         tc_fence_after();
-        uint32_t s[KN];
+        uint32_t s[KC];
         // keys past the end of the sequence (or past this row's causal
-        // limit) in this tile are masked
-        const int lim = klim - (ui.jb + j) * KN;
+        // limit) in this tile are masked: column c of this half is key
+        // h KC + c of the tile
+        const int lim = klim - (ui.jb + j) * KN - h * KC;
         // warp-uniform: both branches below hold tcgen05.wait::ld, which the
-        // whole warp must execute together; masking at lim >= KN is a no-op
-        const bool tail = __any_sync(0xffffffffu, lim < KN);
-        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-        tmem_wait_ld();
-        reg_fence(s, 0, 64);
-        if constexpr (KN >= 96) tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-        if constexpr (KN == 112) tmem_ld16(tS + 96, *reinterpret_cast<uint32_t(*)[16]>(&s[96]));
-        if constexpr (KN == 128) tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+        // whole warp must execute together; masking at lim >= KC is a no-op
+        const bool tail = __any_sync(0xffffffffu, lim < KC);
         float mx0, mx1, mx2, mx3;
-        if (!tail) {
-          // row max of the first 64 keys while the rest is in flight
-          mx0 = __uint_as_float(s[0]);
-          mx1 = __uint_as_float(s[1]);
-          mx2 = __uint_as_float(s[2]);
-          mx3 = __uint_as_float(s[3]);
+        auto max_cols = [&](int c0, int c1) {
 #pragma unroll
-          for (int c = 4; c < 64; c += 8) {
+          for (int c = c0; c < c1; c += 8) {
             mx0 = fmax3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
             mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
             mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
             mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
           }
+        };
+        mx0 = mx1 = mx2 = mx3 = -INFINITY;
+        if constexpr (KC > 64) {
+          // the first 64 columns, then the rest while their max is taken
+          tmem_ld_cols<64>(tS, s);
           tmem_wait_ld();
-          reg_fence(s, 64, KN - 64);
+          reg_fence(s, 0, 64);
+          tmem_ld_cols<KC - 64>(tS + 64, s + 64);
+          if (!tail) {
+            max_cols(0, 64);
+            tmem_wait_ld();
+            reg_fence(s, 64, KC - 64);
+          } else {
+            tmem_wait_ld();
+            reg_fence(s, 64, KC - 64);
+#pragma unroll
+            for (int c = 0; c < KC; ++c)
+              if (c >= lim) s[c] = __float_as_uint(-INFINITY);
+            max_cols(0, 64);
+          }
         } else {
+          tmem_ld_cols<KC>(tS, s);
           tmem_wait_ld();
-          reg_fence(s, 64, KN - 64);
+          reg_fence(s, 0, KC);
+          if (tail) {
 #pragma unroll
-          for (int c = 0; c < KN; ++c)
-            if (c >= lim) s[c] = __float_as_uint(-INFINITY);
-          mx0 = mx1 = mx2 = mx3 = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 64; c += 8) {
-            mx0 = fmax3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-            mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
-            mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
-            mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+            for (int c = 0; c < KC; ++c)
+              if (c >= lim) s[c] = __float_as_uint(-INFINITY);
           }
+          max_cols(0, KC);
         }
         if constexpr (G::PSEP) {
           // S_t is in registers: the MMA warp may compute the next S_t now
           tc_fence_before();
           mbar_arrive(bar(G::B_S_FREE + t));
         }
-#pragma unroll
-        for (int c = 64; c < KN; c += 8) {
-          mx0 = fmax3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-          mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
-          mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
-          mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+        if constexpr (KC > 64) max_cols(64, KC);
+        float mx = fmax3(mx0, mx1, fmaxf(mx2, mx3));
+        if constexpr (H == 2) {
+          bool okx;
+          const float other = exchange(mx, okx);
+          if (!(ok = okx)) break;
+          mx = fmaxf(mx, other);
         }
-        const float mxs = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+        const float mxs = mx * sl2;
         if (j == 0) {
           // a row that sees no key keeps m = 0: all its weights are 0
           m = mxs == -INFINITY ? 0.f : mxs;
@@ -1192,6 +1271,7 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
             l *= alpha;
 #pragma unroll
             for (int c = 0; c < G::DP; c += 16) {
+              if (!mine(c)) continue;
               uint32_t o[16];
               tmem_ld16(tO + c, o);
               tmem_wait_ld();
@@ -1203,12 +1283,13 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
             tmem_wait_st();
           }
         }
-        // p = 2^(s * scale * log2(e) - m), packed two lanes per FMA/add
+        // p = 2^(s * scale * log2(e) - m), packed two lanes per FMA/add;
+        // exp_pairs(c0, c1, pk) fills pk[0, c1 - c0) with packed columns
+        // [c0, c1) (keys 2 c0 ... 2 c1 - 1 of this thread's columns)
         const float2 c2 = make_float2(sl2, sl2);
         const float2 nm2 = make_float2(-m, -m);
         float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-        uint32_t pk[KN / 2];
-        auto exp_pairs = [&](int c0, int c1) {
+        auto exp_pairs = [&](int c0, int c1, uint32_t* pk) {
 #pragma unroll
           for (int c = c0; c < c1; c += 2) {
             float2 a = __ffma2_rn(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])),
@@ -1226,35 +1307,49 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
               b.x = ex2(b.x);
               b.y = ex2(b.y);
             }
-            acc0 = __fadd2_rn(acc0, a);
-            acc1 = __fadd2_rn(acc1, b);
-            pk[c] = pack_bf16x2(a.x, a.y);
-            pk[c + 1] = pack_bf16x2(b.x, b.y);
+            if constexpr (!G::LO) {
+              acc0 = __fadd2_rn(acc0, a);
+              acc1 = __fadd2_rn(acc1, b);
+            }
+            pk[c - c0] = pack_bf16x2(a.x, a.y);
+            pk[c - c0 + 1] = pack_bf16x2(b.x, b.y);
           }
         };
-        if constexpr (G::PSEP) {
-          exp_pairs(0, KN / 2);
+        if constexpr (G::PSEP && (H == 2 || ATTN_VARLEN_P_CHUNKS)) {
+          // P_t(j-1) must have been read by its P.V before it is overwritten;
+          // then P goes out in chunks of 8 packed columns as it is computed
+          // (fewer live registers than the whole row of packed values)
+          if (p_cnt > 0 && !(ok = wait_(bar(G::B_PV_DONE + t), (p_cnt - 1) & 1u))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < KC / 2; c0 += 8) {
+            uint32_t pk[8];
+            if (c0 + 8 <= KC / 2) {
+              exp_pairs(c0, c0 + 8, pk);
+              tmem_st8(tP + c0, *reinterpret_cast<const uint32_t(*)[8]>(pk));
+            } else {
+              exp_pairs(c0, c0 + 4, pk);
+              tmem_st4(tP + c0, *reinterpret_cast<const uint32_t(*)[4]>(pk));
+            }
+          }
+        } else if constexpr (G::PSEP) {
+          uint32_t pk[KC / 2];
+          exp_pairs(0, KC / 2, pk);
           // P_t(j-1) must have been read by its P.V before it is overwritten
           if (p_cnt > 0 && !(ok = wait_(bar(G::B_PV_DONE + t), (p_cnt - 1) & 1u))) break;
           tc_fence_after();
-          // KN / 2 packed columns: 32 + (16 | 16 + 8 | 32)
-          tmem_st32(tP + 0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-          if constexpr (KN == 96 || KN == 112)
-            tmem_st16(tP + 32, *reinterpret_cast<const uint32_t(*)[16]>(&pk[32]));
-          if constexpr (KN == 112)
-            tmem_st8(tP + 48, *reinterpret_cast<const uint32_t(*)[8]>(&pk[48]));
-          if constexpr (KN == 128)
-            tmem_st32(tP + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+          tmem_st_cols<KC / 2>(tP, pk);
         } else {
           // P_t overwrites the first half of S_t, already in registers
 #pragma unroll
-          for (int h = 0; h < KN / 64; ++h) {
-            exp_pairs(32 * h, 32 * h + 32);
-            tmem_st32(tP + 32 * h, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * h]));
+          for (int hh = 0; hh < KN / 64; ++hh) {
+            uint32_t pk[32];
+            exp_pairs(32 * hh, 32 * hh + 32, pk);
+            tmem_st32(tP + 32 * hh, *reinterpret_cast<const uint32_t(*)[32]>(pk));
           }
         }
         tmem_wait_st();
-        l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+        if constexpr (!G::LO) l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
         tc_fence_before();
         mbar_arrive(bar(G::B_P_FULL + t));
         ++p_cnt;
@@ -1263,14 +1358,37 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       // epilogue: O / l -> bf16 -> out (rows of this sequence only)
       if (!(ok = wait_(bar(G::B_PV_DONE + t), (p_cnt - 1) & 1u))) break;
       tc_fence_after();
+      if constexpr (G::LO) {
+        // the row sum is O column D (the ones column of V)
+        uint32_t o[16];
+        tmem_ld16(tO + (D / 16) * 16, o);
+        tmem_wait_ld();
+        reg_fence(o, 0, 16);
+        l = __uint_as_float(o[D % 16]);
+      }
       if (ui.part >= 0) {
-        split_epilogue<D>(p.split + SL.parts, reinterpret_cast<int*>(p.split + SL.counters), tO, t,
-                          r, m, l, orow, valid, ui.part, ui.part0, ui.tail, ui.chunks);
+        split_store<D>(p.split + SL.parts, tO, t, r, h, ui.part);
+        if constexpr (H == 2) {
+          // also orders the other half's partial stores before half 0's count
+          bool okx;
+          const float lo = exchange(l, okx);
+          if (!(ok = okx)) break;
+          if constexpr (!G::LO) l += lo;
+        }
+        if (h == 0)
+          split_finish<D>(p.split + SL.parts, reinterpret_cast<int*>(p.split + SL.counters), t, r,
+                          m, l, orow, valid, ui.part, ui.part0, ui.tail, ui.chunks);
         continue;
+      }
+      if constexpr (H == 2 && !G::LO) {
+        bool okx;
+        l += exchange(l, okx);
+        if (!(ok = okx)) break;
       }
       const float inv = l > 0.f ? 1.0f / l : 0.f;
 #pragma unroll
       for (int c = 0; c < G::DP; c += 16) {
+        if (!mine(c)) continue;
         uint32_t o[16];
         tmem_ld16(tO + c, o);
         tmem_wait_ld();
@@ -1287,11 +1405,10 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       }
     }
   }
-
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == G::MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -180,6 +180,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -209,6 +216,40 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
+// N consecutive 32-bit columns from TMEM (pieces of 32, 16 and 8; N a
+// multiple of 8), starting at r[0].  Completes at the next tmem_wait_ld.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
+  static_assert(N % 8 == 0, "columns");
+#pragma unroll
+  for (int c = 0; c + 32 <= N; c += 32) tmem_ld32(taddr + c, *reinterpret_cast<uint32_t(*)[32]>(r + c));
+  constexpr int c16 = N / 32 * 32;
+  if constexpr (N % 32 >= 16) tmem_ld16(taddr + c16, *reinterpret_cast<uint32_t(*)[16]>(r + c16));
+  constexpr int c8 = N / 16 * 16;
+  if constexpr (N % 16 == 8) tmem_ld8(taddr + c8, *reinterpret_cast<uint32_t(*)[8]>(r + c8));
+}
+
+// N consecutive 32-bit columns to TMEM (pieces of 32, 16, 8 and 4).
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) {
+  static_assert(N % 4 == 0, "columns");
+#pragma unroll
+  for (int c = 0; c + 32 <= N; c += 32)
+    tmem_st32(taddr + c, *reinterpret_cast<const uint32_t(*)[32]>(r + c));
+  constexpr int c16 = N / 32 * 32;
+  if constexpr (N % 32 >= 16) tmem_st16(taddr + c16, *reinterpret_cast<const uint32_t(*)[16]>(r + c16));
+  constexpr int c8 = N / 16 * 16;
+  if constexpr (N % 16 >= 8) tmem_st8(taddr + c8, *reinterpret_cast<const uint32_t(*)[8]>(r + c8));
+  constexpr int c4 = N / 8 * 8;
+  if constexpr (N % 8 == 4) tmem_st4(taddr + c4, *reinterpret_cast<const uint32_t(*)[4]>(r + c4));
 }
 
 // ------------------------------------------------------------ descriptors
