@@ -104,17 +104,9 @@ constexpr int kMergeTiles = 8;
 
 // K/V ring depth per head_dim (shared memory: head_dim 72 holds 2 x 18 KB of
 // Q and 16 KB per stage, head_dim 128 2 x 32 KB and 32 KB per stage)
-#ifndef ATTN_VARLEN_HALVES
-#define ATTN_VARLEN_HALVES 1
-#endif
 // head_dim 72: the row sum of P comes out of the P.V product as O column 72
 // (V's padding column 72 reads 1.0 from a "ones" region), instead of being
 // added up by the softmax threads.
-// Store P in chunks of 8 packed columns as they are computed (always with
-// HALVES = 2; optional with one thread per row).
-#ifndef ATTN_VARLEN_P_CHUNKS
-#define ATTN_VARLEN_P_CHUNKS 0
-#endif
 #ifndef ATTN_VARLEN_SUM_IN_O
 #define ATTN_VARLEN_SUM_IN_O 1
 #endif
@@ -215,15 +207,9 @@ struct Geometry {
   static constexpr bool PSEP = Cfg<D>::PSEP;
   static constexpr int ISSUERS = Cfg<D>::ISSUERS;
   static_assert(PSEP || ISSUERS == 1, "two issuers need P in columns of its own");
-  // Softmax threads per Q-tile row: with HALVES = 2 two threads share each
-  // row, one per half of the key tile's columns (four softmax warps per SM
-  // sub-partition instead of two, to hide the latency of each row's chain).
-  static constexpr int HALVES = PSEP ? ATTN_VARLEN_HALVES : 1;
-  static_assert(HALVES == 1 || HALVES == 2, "halves");
-  static constexpr int KC = KN / HALVES;                  // key columns per softmax thread
-  static constexpr int SM_WARPS = 8 * HALVES;             // softmax warps: 2 tiles x HALVES x 4
-  static constexpr int LOAD_WARP = SM_WARPS;              // TMA producer
-  static constexpr int MMA_WARP = SM_WARPS + 1;           // first MMA issuer (and TMEM owner)
+  static constexpr int SM_WARPS = 8;             // softmax warps: 2 Q tiles x 4
+  static constexpr int LOAD_WARP = SM_WARPS;     // TMA producer
+  static constexpr int MMA_WARP = SM_WARPS + 1;  // first MMA issuer (and TMEM owner)
   static constexpr int THREADS = 32 * (MMA_WARP + ISSUERS);
   static constexpr int NB = (DP + BW - 1) / BW;             // boxes per tile
   static constexpr int STAGES = Cfg<D>::STAGES;
@@ -259,19 +245,14 @@ struct Geometry {
   static constexpr bool LO = ZB && ATTN_VARLEN_SUM_IN_O != 0;
   static constexpr uint32_t ONES_OFF = ZERO_OFF + ZERO_BYTES;
   static constexpr uint32_t ONES_BYTES = LO ? kBlockM * 16u : 0u;
-  // row-statistics exchange between the two threads of a row (HALVES = 2):
-  // float [2 buffers][2 tiles][2 halves][128 rows]
-  static constexpr uint32_t XCH_OFF = ONES_OFF + ONES_BYTES;
-  static constexpr uint32_t XCH_BYTES = HALVES == 2 ? 2u * 2u * 2u * kBlockM * 4u : 0u;
-  static constexpr uint32_t BAR_OFF = XCH_OFF + XCH_BYTES;
+  static constexpr uint32_t BAR_OFF = ONES_OFF + ONES_BYTES;
   // barrier slots (8 bytes each)
   static constexpr int B_Q_FULL = 0, B_Q_EMPTY = 1, B_KV_FULL = 2, B_KV_EMPTY = 2 + STAGES,
                        B_S_FULL = 2 + 2 * STAGES, B_P_FULL = B_S_FULL + 2,
                        B_PV_DONE = B_P_FULL + 2, B_S_FREE = B_PV_DONE + 2,
                        B_DRAIN = B_S_FREE + 2, B_ITEM_FULL = B_DRAIN + 2,
                        B_ITEM_EMPTY = B_ITEM_FULL + kItemDepth,
-                       B_XCH = B_ITEM_EMPTY + kItemDepth,  // per (tile, lane quarter)
-                       NUM_BARS = B_XCH + (HALVES == 2 ? 8 : 0);
+                       NUM_BARS = B_ITEM_EMPTY + kItemDepth;
   // tmem slot, abort flag, then the item ring (kItemDepth int32)
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = MISC_OFF + 8 + 4 * kItemDepth + 1024;  // + alignment slack
@@ -626,14 +607,11 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
   }
 }
 
-// Epilogue of one chunk of a split unit for one row (softmax threads of Q
-// tile t, row r, column half h), in two steps.  split_store: the
-// unnormalised O row goes to partial slot `part`, each half writing its
-// 16-column chunks.  Then (in the caller) the halves combine their row sums,
-// which also orders the other half's stores before half 0's count, and
-// split_finish (half 0) writes (m, l) and counts the chunk in; the last chunk
-// of the unit to finish that row (a counter per row and Q tile) merges the
-// unit's chunks in chunk order,
+// Epilogue of one chunk of a split unit for one row (softmax thread of Q
+// tile t, row r), in two steps.  split_store: the unnormalised O row goes to
+// partial slot `part`.  split_finish: (m, l) go next to it and the chunk is
+// counted in; the last chunk of the unit to finish that row (a counter per
+// row and Q tile) merges the unit's chunks in chunk order,
 //   m* = max_c m_c,  O = sum_c 2^(m_c - m*) O_c,  l = sum_c 2^(m_c - m*) l_c,
 // and writes O / l as bf16.  No thread waits for another CTA.  A slot is
 // column-major ([column][128 rows]) so that a warp's stores and loads of one
@@ -642,14 +620,11 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
 constexpr size_t kSlot = (size_t)kPartRowMax * kBlockM;  // floats per (chunk, tile) slot
 
 template <int D>
-__device__ __noinline__ void split_store(uint8_t* parts_base, uint32_t tO, int t, int r, int h,
-                                         int part) {
+__device__ __noinline__ void split_store(uint8_t* parts_base, uint32_t tO, int t, int r, int part) {
   using G = Geometry<D>;
-  constexpr int H = G::HALVES;
   float* mine = reinterpret_cast<float*>(parts_base) + (size_t)(part * 2 + t) * kSlot + r;
 #pragma unroll
   for (int c = 0; c < G::DP; c += 16) {
-    if ((c / 16) % H != h) continue;
     uint32_t o[16];
     tmem_ld16(tO + c, o);
     tmem_wait_ld();
@@ -767,9 +742,9 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(G::B_S_FULL + t), 1);
-      mbar_init(bar(G::B_P_FULL + t), kBlockM * G::HALVES);
+      mbar_init(bar(G::B_P_FULL + t), kBlockM);
       mbar_init(bar(G::B_PV_DONE + t), 1);
-      mbar_init(bar(G::B_S_FREE + t), kBlockM * G::HALVES);
+      mbar_init(bar(G::B_S_FREE + t), kBlockM);
     }
     mbar_init(bar(G::B_DRAIN + 0), 1);
     mbar_init(bar(G::B_DRAIN + 1), 1);
@@ -777,8 +752,6 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       mbar_init(bar(G::B_ITEM_FULL + i), 1);
       mbar_init(bar(G::B_ITEM_EMPTY + i), G::ITEM_CONSUMERS);
     }
-    if (G::HALVES == 2)
-      for (int i = 0; i < 8; ++i) mbar_init(bar(G::B_XCH + i), 64);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1129,45 +1102,24 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
     }
   } else {
     // --------------------------------------------------------- softmax
-    // Warp w: Q tile t = w / (4 H), column half h = (w / 4) mod H, TMEM lane
-    // quarter w mod 4.  Each thread owns row r of its tile (TMEM lane r) and
-    // the KC = KN / H key columns [h KC, (h + 1) KC) of every key tile.  With
-    // H = 2 the two threads of a row combine their partial row maxima every
-    // key tile, and their partial row sums once per unit, through shared
-    // memory and one mbarrier per (tile, lane quarter), whose waits are
-    // bounded like every other wait.  Output columns are handed out in
-    // 16-column chunks: chunk c / 16 belongs to half (c / 16) mod H.
-    constexpr int KN = G::KN, H = G::HALVES, KC = G::KC;
-    const int t = warp / (4 * H);                  // Q tile of this warp
-    const int h = (warp >> 2) % H;                 // column half
+    // Warp w: Q tile t = w / 4, TMEM lane quarter w mod 4; each thread owns
+    // row r of its tile (TMEM lane r) and all KN key columns of every tile.
+    constexpr int KN = G::KN, KC = KN;
+    const int t = warp >> 2;                       // Q tile of this warpgroup
     const int qq = warp & 3;                       // TMEM lane quarter
-    const int r = (qq << 5) | (threadIdx.x & 31);  // row in the tile = TMEM lane
+    const int r = threadIdx.x & 127;               // row in the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + G::s_col(t) + (uint32_t)(h * KC);
-    const uint32_t tP = tmem + lane_off + G::p_col(t) + (uint32_t)(h * KC / 2);
+    const uint32_t tS = tmem + lane_off + G::s_col(t);
+    const uint32_t tP = tmem + lane_off + G::p_col(t);
     const uint32_t tO = tmem + lane_off + G::o_col(t);
     const float sl2 = p.scale_log2;
-    uint32_t s_wait = 0, p_cnt = 0, x_use = 0;
+    uint32_t s_wait = 0, p_cnt = 0;
     bool ok = true;
 
     auto wait_ = [&](uint32_t b, uint32_t parity) -> bool {
       bool w = wait_bounded(b, parity, abort_flag, p.status, kStatusTimeoutSoftmax);
       return __all_sync(0xffffffffu, w);
     };
-    // H = 2: hand v to the other thread of this row and return its value.
-    // Two buffers alternate; a buffer is rewritten two exchanges later, after
-    // the partner has passed the next exchange and so finished reading it.
-    float* xch = reinterpret_cast<float*>(base_ptr + G::XCH_OFF);
-    const uint32_t xbar = bar(G::B_XCH + 4 * t + qq);
-    auto exchange = [&](float v, bool& okx) -> float {
-      float* slot = xch + (size_t)(((x_use & 1u) * 2u + (uint32_t)t) * H) * kBlockM;
-      slot[h * kBlockM + r] = v;
-      mbar_arrive(xbar);  // release: the store is visible to whoever sees the phase
-      okx = wait_(xbar, x_use & 1u);
-      ++x_use;
-      return slot[(1 - h) * kBlockM + r];
-    };
-    auto mine = [&](int c) { return (c / 16) % H == h; };  // 16-column output chunk
 
     for (int k = 0; ok; ++k) {
       const int u = next_item(k);
@@ -1185,8 +1137,7 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       if (nsteps == 0) {
         if (valid) {
 #pragma unroll
-          for (int c = 0; c < D; c += 8)
-            if (mine(c)) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -1197,9 +1148,8 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
         tc_fence_after();
         uint32_t s[KC];
         // keys past the end of the sequence (or past this row's causal
-        // limit) in this tile are masked: column c of this half is key
-        // h KC + c of the tile
-        const int lim = klim - (ui.jb + j) * KN - h * KC;
+        // limit) in this tile are masked
+        const int lim = klim - (ui.jb + j) * KN;
         // warp-uniform: both branches below hold tcgen05.wait::ld, which the
         // whole warp must execute together; masking at lim >= KC is a no-op
         const bool tail = __any_sync(0xffffffffu, lim < KC);
@@ -1249,14 +1199,7 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
           mbar_arrive(bar(G::B_S_FREE + t));
         }
         if constexpr (KC > 64) max_cols(64, KC);
-        float mx = fmax3(mx0, mx1, fmaxf(mx2, mx3));
-        if constexpr (H == 2) {
-          bool okx;
-          const float other = exchange(mx, okx);
-          if (!(ok = okx)) break;
-          mx = fmaxf(mx, other);
-        }
-        const float mxs = mx * sl2;
+        const float mxs = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
         if (j == 0) {
           // a row that sees no key keeps m = 0: all its weights are 0
           m = mxs == -INFINITY ? 0.f : mxs;
@@ -1271,7 +1214,6 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
             l *= alpha;
 #pragma unroll
             for (int c = 0; c < G::DP; c += 16) {
-              if (!mine(c)) continue;
               uint32_t o[16];
               tmem_ld16(tO + c, o);
               tmem_wait_ld();
@@ -1315,24 +1257,7 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
             pk[c - c0 + 1] = pack_bf16x2(b.x, b.y);
           }
         };
-        if constexpr (G::PSEP && (H == 2 || ATTN_VARLEN_P_CHUNKS)) {
-          // P_t(j-1) must have been read by its P.V before it is overwritten;
-          // then P goes out in chunks of 8 packed columns as it is computed
-          // (fewer live registers than the whole row of packed values)
-          if (p_cnt > 0 && !(ok = wait_(bar(G::B_PV_DONE + t), (p_cnt - 1) & 1u))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int c0 = 0; c0 < KC / 2; c0 += 8) {
-            uint32_t pk[8];
-            if (c0 + 8 <= KC / 2) {
-              exp_pairs(c0, c0 + 8, pk);
-              tmem_st8(tP + c0, *reinterpret_cast<const uint32_t(*)[8]>(pk));
-            } else {
-              exp_pairs(c0, c0 + 4, pk);
-              tmem_st4(tP + c0, *reinterpret_cast<const uint32_t(*)[4]>(pk));
-            }
-          }
-        } else if constexpr (G::PSEP) {
+        if constexpr (G::PSEP) {
           uint32_t pk[KC / 2];
           exp_pairs(0, KC / 2, pk);
           // P_t(j-1) must have been read by its P.V before it is overwritten
@@ -1367,28 +1292,14 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
         l = __uint_as_float(o[D % 16]);
       }
       if (ui.part >= 0) {
-        split_store<D>(p.split + SL.parts, tO, t, r, h, ui.part);
-        if constexpr (H == 2) {
-          // also orders the other half's partial stores before half 0's count
-          bool okx;
-          const float lo = exchange(l, okx);
-          if (!(ok = okx)) break;
-          if constexpr (!G::LO) l += lo;
-        }
-        if (h == 0)
-          split_finish<D>(p.split + SL.parts, reinterpret_cast<int*>(p.split + SL.counters), t, r,
-                          m, l, orow, valid, ui.part, ui.part0, ui.tail, ui.chunks);
+        split_store<D>(p.split + SL.parts, tO, t, r, ui.part);
+        split_finish<D>(p.split + SL.parts, reinterpret_cast<int*>(p.split + SL.counters), t, r, m,
+                        l, orow, valid, ui.part, ui.part0, ui.tail, ui.chunks);
         continue;
-      }
-      if constexpr (H == 2 && !G::LO) {
-        bool okx;
-        l += exchange(l, okx);
-        if (!(ok = okx)) break;
       }
       const float inv = l > 0.f ? 1.0f / l : 0.f;
 #pragma unroll
       for (int c = 0; c < G::DP; c += 16) {
-        if (!mine(c)) continue;
         uint32_t o[16];
         tmem_ld16(tO + c, o);
         tmem_wait_ld();
