@@ -12,8 +12,11 @@ under "shapes".  Metric: TFLOP/s with FLOPs = 4 * sum(L_q * L_k) * H * D
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Under torchrun (N > 1) every rank runs the same workload on its own GPU (weak
-scaling, no collective on the data path); rank 0 prints the JSON line.
+Under torchrun (N > 1) the ranks split the heads of the workload (strong
+scaling: the whole job is one call's worth of work): rank r computes its
+contiguous block of heads in place with attn_varlen_fwd_heads, with no
+collective on the data path; the slowest rank sets the time and rank 0
+prints the JSON line.
 """
 from __future__ import annotations
 
@@ -216,7 +219,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": secs / max(args.steps, 1) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w),
+            "config": workload_config(w, world),
             "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": runs[0]["cores"] if runs else None,
                              "kind": "oracle",
                              "sample": f"{rows} seeded (token, head) rows of {w.name}, all keys "
@@ -236,10 +239,11 @@ def max_over_ranks(x: float, device) -> float:
     return float(t.item())
 
 
-def whole_job_throughput(flops_per_step: float, steps: int, world: int, seconds: float) -> float:
-    """TFLOP/s of all ranks together: every rank runs the same workload
-    (weak scaling), timed by the slowest rank."""
-    return flops_per_step * steps * world / seconds / 1e12
+def whole_job_throughput(job_flops_per_step: float, steps: int, seconds: float) -> float:
+    """TFLOP/s of all ranks together: ``job_flops_per_step`` is the work all
+    ranks do in one step together (the ranks split one workload's heads),
+    timed by the slowest rank."""
+    return job_flops_per_step * steps / seconds / 1e12
 
 
 def time_calls(fn, steps, flush_buf, stream):
@@ -314,10 +318,11 @@ def run_profile_chunk(args):
           flush=True)
 
 
-def workload_config(w) -> dict:
+def workload_config(w, world: int = 1) -> dict:
     """The JSON line's config for workload w (both arms print the same)."""
     return {"workload": w.name, "seq_lens": list(w.seq_lens_q), "num_heads": w.num_heads,
-            "head_dim": w.head_dim, "l2": "flushed before every step (256 MiB write)"}
+            "head_dim": w.head_dim, "l2": "flushed before every step (256 MiB write)",
+            "parallelism": f"heads split over {world} GPU(s)"}
 
 
 def percentiles_us(durs_ms) -> dict:
@@ -383,7 +388,10 @@ def run_ours(args, rank, world, local_rank):
     w = CONFIGS[args.workload] if args.workload else HEADLINE
     x, t, cu_q, cu_k = device_inputs(w)
     out = torch.empty_like(t["q"])
-    step = lambda: vlp.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, out=out)  # noqa: E731
+    # this rank's heads (all of them on one GPU)
+    shard = vlp.head_shard(w.num_heads, rank, world) if world > 1 else None
+    step = lambda: vlp.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, out=out,  # noqa: E731
+                                       heads=shard)
     for _ in range(args.warmup):
         step()
     vlp.check()
@@ -401,10 +409,10 @@ def run_ours(args, rank, world, local_rank):
                               "ms_per_step": sum(durs) / args.steps}), flush=True)
         return
     t_sum = max_over_ranks(sum(durs) / 1e3, dev)  # seconds of device time over the K steps
-    flops = w.flops()
-    value = whole_job_throughput(flops, args.steps, world, t_sum)
+    flops = w.flops()  # the whole job's work per step (all ranks together)
+    value = whole_job_throughput(flops, args.steps, t_sum)
     ms_per_step = t_sum / args.steps * 1e3
-    per_call_tflops = flops / (t_sum / args.steps) / 1e12
+    per_call_tflops = flops / world / (t_sum / args.steps) / 1e12  # one GPU's kernel rate
 
     # end to end through the public API with host buffers (pinned), copies included
     host = {n: torch.from_numpy(x[n].view(np.int16)).pin_memory() for n in ("q", "k", "v")}
@@ -422,7 +430,7 @@ def run_ours(args, rank, world, local_rank):
         dv.view(torch.int16).copy_(host["v"], non_blocking=True)
         dcq.copy_(hcu_q, non_blocking=True)
         dck.copy_(hcu_k, non_blocking=True)
-        vlp.attn_varlen_fwd(dq, dk, dv, dcq, dck, out=out)
+        vlp.attn_varlen_fwd(dq, dk, dv, dcq, dck, out=out, heads=shard)
         hout.copy_(out.view(torch.int16), non_blocking=True)
 
     for _ in range(2):
@@ -430,8 +438,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_steps = max(3, min(args.steps, 20))
     e2e_durs = time_calls(e2e_step, e2e_steps, None, stream)
-    e2e_value = whole_job_throughput(flops, e2e_steps, world,
-                                     max_over_ranks(sum(e2e_durs) / 1e3, dev))
+    e2e_value = whole_job_throughput(flops, e2e_steps, max_over_ranks(sum(e2e_durs) / 1e3, dev))
     del dq, dk, dv, host, hout
 
     # The second full record and every workload once more, under one clock
@@ -556,11 +563,11 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak",
+        "higher_is_better": True, "scaling": "strong",
         # the page's T_Prod for this workload (other, unnamed hardware): context
-        "vs_baseline": round(value / world / tprod, 3) if tprod else None,
+        "vs_baseline": round(value / tprod, 3) if tprod else None,
         "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(w),
+        "config": workload_config(w, world),
         **{k: v for k, v in percentiles_us(durs).items() if k != "us"},
         "roofline": roofline_block(w, per_call_tflops, peaks, kernel_name(w)),
         "cpu_baseline": {"value": cpu["tflops"], "unit": "TFLOP/s", "cores": cpu["cores"],

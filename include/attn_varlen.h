@@ -103,6 +103,30 @@ int attn_varlen_fwd_causal(const void* q, const void* k, const void* v,
                            int num_seqs, int num_heads, int head_dim,
                            void* out, cudaStream_t stream);
 
+/*
+ * attn_varlen_fwd_heads -- heads [head_begin, head_begin + head_count) only.
+ *
+ * The same operation as attn_varlen_fwd (causal != 0: attn_varlen_fwd_causal)
+ * restricted to a contiguous range of heads of the same packed tensors: q, k,
+ * v and out are the whole [total, num_heads, head_dim] buffers, read and
+ * written in place; out rows of heads outside the range are not touched.
+ * Heads are independent in this operation (each head's output depends on its
+ * own q, k and v slices only), so G processes (one per GPU, each with a copy
+ * of the inputs) can split the heads between them with no exchange, and
+ * the output needs gathering only if one process wants it whole.
+ *
+ *   head_begin, head_count   0 <= head_begin, head_begin + head_count <=
+ *                            num_heads; head_count 0 returns ATTN_VARLEN_OK
+ *                            without launching anything
+ *
+ * Other arguments, the workspace and the errors are those of attn_varlen_fwd
+ * (ATTN_VARLEN_ERR_INVALID_ARG for a range outside [0, num_heads)).
+ */
+int attn_varlen_fwd_heads(const void* q, const void* k, const void* v,
+                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                          int num_seqs, int num_heads, int head_begin, int head_count,
+                          int head_dim, int causal, void* out, cudaStream_t stream);
+
 /* Bytes of workspace attn_varlen_fwd_ws needs for num_seqs sequences
  * (0 for num_seqs < 0). */
 size_t attn_varlen_workspace_size(int num_seqs);

@@ -90,6 +90,23 @@ def test_argument_checks_need_no_gpu(args, code):
     assert vlp.load().attn_varlen_fwd(*args) == code
 
 
+@pytest.mark.parametrize("args,code", [
+    # (q, k, v, cu_q, cu_k, num_seqs, H, head_begin, head_count, D, causal, out, stream)
+    ((P, P, P, P, P, 1, 4, -1, 2, 72, 0, P, None), B.ERR_INVALID_ARG),
+    ((P, P, P, P, P, 1, 4, 3, 2, 72, 0, P, None), B.ERR_INVALID_ARG),
+    ((P, P, P, P, P, 1, 4, 0, -1, 72, 0, P, None), B.ERR_INVALID_ARG),
+    ((P, P, P, P, P, 1, 4, 5, 0, 72, 0, P, None), B.ERR_INVALID_ARG),
+    ((P, P, P, P, P, 1, 0, 0, 0, 72, 0, P, None), B.ERR_INVALID_ARG),
+    ((P, P, P, P, P, 1, 4, 0, 4, 48, 1, P, None), B.ERR_UNSUPPORTED_DIM),
+    ((P + 8, P, P, P, P, 1, 4, 0, 4, 72, 0, P, None), B.ERR_MISALIGNED),
+    # an empty head range or no sequence is a no-op
+    ((P, P, P, P, P, 1, 4, 2, 0, 72, 0, P, None), B.OK),
+    ((None, None, None, None, None, 0, 4, 0, 4, 72, 0, None, None), B.OK),
+])
+def test_head_range_checks_need_no_gpu(args, code):
+    assert vlp.load().attn_varlen_fwd_heads(*args) == code
+
+
 def test_workspace_variant_checks():
     lib = vlp.load()
     need = vlp.workspace_size(2)

@@ -1,5 +1,5 @@
 """bench.py's multi-rank timing on CPU: two gloo ranks, the slowest rank's
-time sets the whole-job throughput (weak scaling)."""
+time sets the whole-job throughput (the ranks split one workload)."""
 import os
 import sys
 
@@ -18,7 +18,7 @@ def _rank(rank, world, port, q):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         t = bench.max_over_ranks(1.0 + rank, "cpu")
-        v = bench.whole_job_throughput(1e12, 10, world, t)
+        v = bench.whole_job_throughput(2e12, 10, t)
         q.put((rank, t, v))
     finally:
         dist.destroy_process_group()
@@ -37,11 +37,11 @@ def test_two_gloo_ranks_take_the_slowest_time():
     res = sorted(q.get(timeout=10) for _ in range(2))
     for rank, t, v in res:
         assert t == 2.0                       # max over ranks
-        assert v == pytest.approx(1e12 * 10 * 2 / 2.0 / 1e12)  # 10 TFLOP/s job-wide
+        assert v == pytest.approx(2e12 * 10 / 2.0 / 1e12)  # 10 TFLOP/s job-wide
 
 
 def test_single_process_needs_no_group():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.max_over_ranks(3.5, "cpu") == 3.5
-    assert bench.whole_job_throughput(2e12, 4, 1, 2.0) == pytest.approx(4.0)
+    assert bench.whole_job_throughput(2e12, 4, 2.0) == pytest.approx(4.0)

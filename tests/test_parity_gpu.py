@@ -118,6 +118,45 @@ def test_backwards_cu_seqlens(cuda_lib, D, causal, ws):
                  bound=bound)
 
 
+@pytest.mark.parametrize("D,causal", [(72, False), (128, False), (64, True)])
+def test_head_shards_in_place(cuda_lib, D, causal):
+    """attn_varlen_fwd_heads on the shards of a 5-head batch: one shard
+    leaves the other heads' rows untouched (a sentinel survives bit for bit),
+    and the three shards of a 3-way split together meet the bar against the
+    oracle on every head."""
+    import torch
+    from variable_length_prefill_gb300 import head_shard
+    w = Workload(f"heads_{D}", (300, 1, 0, 700), 5, D, seed=95 + D, seq_lens_k=(300, 40, 3, 700))
+    x = make_inputs(w)
+    t, cu_q, cu_k = device_inputs(x, "cuda")
+    sentinel = 0x7FC1
+    out = torch.full(t["q"].shape, sentinel, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    b, c = head_shard(5, 1, 2)
+    cuda_lib.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, out=out, causal=causal,
+                             heads=(b, c))
+    cuda_lib.check()
+    got = to_bits(out)
+    live = np.zeros(got.shape[0], bool)
+    cu = x["cu_q"]
+    for i in range(len(cu) - 1):
+        live[cu[i]:cu[i + 1]] = cu[i + 1] > cu[i]
+    others = [h for h in range(5) if not b <= h < b + c]
+    assert (got[:, others] == sentinel).all()
+    assert (got[live][:, b:b + c] != sentinel).all()
+    cuda_lib.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, out=out, causal=causal,
+                             heads=(2, 0))  # an empty range writes nothing
+    for r in range(3):
+        cuda_lib.attn_varlen_fwd(t["q"], t["k"], t["v"], cu_q, cu_k, out=out, causal=causal,
+                                 heads=head_shard(5, r, 3))
+    cuda_lib.check()
+    got = to_bits(out)
+    ref = oracle.attn_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], causal=causal)
+    absv = oracle.attn_varlen(x["q"], x["k"], abs_bits(x["v"]), x["cu_q"], x["cu_k"],
+                              causal=causal)
+    assert_close(got[live], ref[live], f"head shards D={D} causal={causal}",
+                 bound=bf16_bound(ref[live], absv[live]))
+
+
 def test_num_seqs_zero_is_a_noop(cuda_lib):
     import torch
     q = torch.zeros(4, 2, 72, dtype=torch.bfloat16, device="cuda")

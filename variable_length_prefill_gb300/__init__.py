@@ -13,7 +13,8 @@ from ._binding import (AttnVarlenError, SYMBOLS, attn_varlen_fwd, attn_varlen_fw
                        check, chunk_delta_rule_output, load, paged_attn_decode, strerror,
                        workspace_size)
 from .build import build, lib_path
+from .shard import head_shard
 
 __all__ = ["AttnVarlenError", "SYMBOLS", "attn_varlen_fwd", "attn_varlen_fwd_noalloc", "build",
-           "check", "chunk_delta_rule_output", "lib_path", "load", "paged_attn_decode", "strerror",
-           "workspace_size"]
+           "check", "chunk_delta_rule_output", "head_shard", "lib_path", "load",
+           "paged_attn_decode", "strerror", "workspace_size"]

@@ -40,6 +40,7 @@ SYMBOLS = {
     "attn_varlen_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "attn_varlen_last_cuda_error": (ctypes.c_char_p, []),
     "attn_varlen_fwd_causal": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "attn_varlen_fwd_heads": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "paged_attn_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "chunk_delta_rule_output": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                      ctypes.c_float, _P, _P]),
@@ -112,7 +113,7 @@ def _check_inputs(q, k, v, cu_q, cu_k, out):
 
 
 def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, out=None, stream=None,
-                    workspace=None, causal=False):
+                    workspace=None, causal=False, heads=None):
     """softmax(q k^T / sqrt(head_dim)) v per packed sequence and head.
 
     q: bf16 [total_q, H, D]; k, v: bf16 [total_k, H, D]; cu_seqlens_q/k:
@@ -121,7 +122,9 @@ def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, out=None, stream=None,
     left untouched).  ``workspace``: optional uint8 CUDA tensor of at least
     ``workspace_size(num_seqs)`` bytes, zero-filled before first use.
     ``causal``: row r of a sequence sees keys j <= r + L_k - L_q
-    (attn_varlen_fwd_causal; library-owned workspace only).
+    (attn_varlen_fwd_causal; library-owned workspace only).  ``heads``: a
+    ``(head_begin, head_count)`` pair to compute only those heads of the
+    same tensors in place (attn_varlen_fwd_heads; library-owned workspace).
     """
     import torch
     if out is None:
@@ -131,10 +134,15 @@ def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, out=None, stream=None,
     num_seqs = cu_seqlens_q.numel() - 1
     H, D = q.shape[1], q.shape[2]
     s = _stream_handle(stream, q.device)
-    if causal and workspace is not None:
-        raise ValueError("the causal entry point uses the library-owned workspace")
+    if (causal or heads is not None) and workspace is not None:
+        raise ValueError("the causal and head-range entry points use the library-owned workspace")
     with torch.cuda.device(q.device):
-        if causal:
+        if heads is not None:
+            rc = lib.attn_varlen_fwd_heads(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                           cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+                                           num_seqs, H, int(heads[0]), int(heads[1]), D,
+                                           1 if causal else 0, out.data_ptr(), s)
+        elif causal:
             rc = lib.attn_varlen_fwd_causal(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                             cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
                                             num_seqs, H, D, out.data_ptr(), s)

@@ -154,10 +154,14 @@ int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[
 namespace {
 
 // `split_cap` > 0: the workspace holds a tail-split region for that many
-// items right after ws_layout(num_seqs).total.
+// items right after ws_layout(num_seqs).total.  Heads [head_begin,
+// head_begin + head_count) of the num_heads-head tensors are computed
+// (head_count < 0: all of them).
 int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const int32_t* cu_k,
         int num_seqs, int num_heads, int head_dim, void* out, void* ws, int split_cap, int dev,
-        DeviceState& st, cudaStream_t stream, bool causal = false) {
+        DeviceState& st, cudaStream_t stream, bool causal = false, int head_begin = 0,
+        int head_count = -1) {
+  if (head_count < 0) head_count = num_heads;
   avp::PlanParams pp;
   std::memset(&pp, 0, sizeof(pp));
   const void* bases[avp::kTensors] = {q, k, v};
@@ -175,7 +179,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const 
   pp.kv_rows = avp::kv_tile_rows(head_dim);
   pp.causal = causal ? 1 : 0;
   pp.num_seqs = num_seqs;
-  pp.num_heads = num_heads;
+  pp.num_heads = head_count;
   pp.row_bytes = num_heads * head_dim * 2;
 
   avp::FwdParams fp;
@@ -188,6 +192,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const 
   fp.out = static_cast<uint16_t*>(out);
   fp.num_seqs = num_seqs;
   fp.num_heads = num_heads;
+  fp.head_begin = head_begin;
   fp.causal = causal ? 1 : 0;
   fp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
   fp.test_withhold = g_test_withhold;
@@ -269,9 +274,10 @@ size_t attn_varlen_workspace_size(int num_seqs) {
 
 static int fwd_owned(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
                      const int32_t* cu_seqlens_k, int num_seqs, int num_heads, int head_dim,
-                     void* out, cudaStream_t stream, bool causal) {
+                     void* out, cudaStream_t stream, bool causal, int head_begin = 0,
+                     int head_count = -1) {
   int rc = check_args(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out);
-  if (rc || num_seqs == 0) return rc;
+  if (rc || num_seqs == 0 || head_count == 0) return rc;
   int dev = 0;
   if ((rc = current_device(&dev))) return rc;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -284,7 +290,7 @@ static int fwd_owned(const void* q, const void* k, const void* v, const int32_t*
   if ((rc = ensure_workspace(st, avp::ws_layout(num_seqs).total + avp::split_layout(cap).total)))
     return rc;
   return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, st.ws, cap,
-             dev, st, stream, causal);
+             dev, st, stream, causal, head_begin, head_count);
 }
 
 int attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
@@ -299,6 +305,17 @@ int attn_varlen_fwd_causal(const void* q, const void* k, const void* v,
                            int num_heads, int head_dim, void* out, cudaStream_t stream) {
   return fwd_owned(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, stream,
                    true);
+}
+
+int attn_varlen_fwd_heads(const void* q, const void* k, const void* v,
+                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int num_seqs,
+                          int num_heads, int head_begin, int head_count, int head_dim, int causal,
+                          void* out, cudaStream_t stream) {
+  if (num_heads < 1 || head_begin < 0 || head_count < 0 || head_begin > num_heads ||
+      head_count > num_heads - head_begin)
+    return ATTN_VARLEN_ERR_INVALID_ARG;
+  return fwd_owned(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, stream,
+                   causal != 0, head_begin, head_count);
 }
 
 int attn_varlen_fwd_ws(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,

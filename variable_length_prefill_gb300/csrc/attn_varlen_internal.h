@@ -93,8 +93,8 @@ struct PlanParams {
   int kv_rows;     // keys per K/V tile
   int causal;      // causal mask: never split units along keys
   int num_seqs;
-  int num_heads;
-  int row_bytes;  // num_heads * head_dim * 2
+  int num_heads;  // heads this call computes (units per 256-row block)
+  int row_bytes;  // tensors' row stride: all heads * head_dim * 2
 };
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -121,7 +121,8 @@ struct FwdParams {
   const int32_t* cu_k;
   uint16_t* out;
   int num_seqs;
-  int num_heads;
+  int num_heads;     // heads of the tensors (their row stride)
+  int head_begin;    // first head this call computes (units cover head_count heads)
   int causal;        // 1: row r of a sequence sees keys <= r + L_k - L_q
   float scale_log2;  // head_dim^-1/2 * log2(e)
   int test_withhold; // read only by test builds (ATTN_VARLEN_TEST_HOOKS); 0 otherwise

@@ -280,11 +280,13 @@ struct UnitInfo {
   bool t1;  // second Q tile holds at least one row
 };
 
+// Unit u -> sequence, head (offset by head_begin: the call may cover a
+// sub-range of the tensors' heads), 256-row block and key-tile range.
 __device__ __forceinline__ UnitInfo decode_unit(int u, const int32_t* __restrict__ order,
                                                 const int32_t* __restrict__ prefix, int num_seqs,
                                                 const int32_t* __restrict__ cu_q,
                                                 const int32_t* __restrict__ cu_k, int kn,
-                                                bool causal) {
+                                                bool causal, int head_begin) {
   // largest rank r in [0, num_seqs) with prefix[r] <= u
   int lo = 0, hi = num_seqs - 1;
   while (lo < hi) {
@@ -300,8 +302,9 @@ __device__ __forceinline__ UnitInfo decode_unit(int u, const int32_t* __restrict
   ui.lk = __ldg(cu_k + ui.seq + 1) - kb;
   if (ui.lk < 0) ui.lk = 0;
   const int pairs = (ui.lq + kUnitRows - 1) / kUnitRows;
-  ui.head = local / pairs;
-  const int qb = local - ui.head * pairs;
+  const int hl = local / pairs;
+  ui.head = head_begin + hl;
+  const int qb = local - hl * pairs;
   // causal: the last row blocks see the most keys, so they go first
   ui.q0 = (causal ? pairs - 1 - qb : qb) * kUnitRows;
   ui.t1 = ui.q0 + kBlockM < ui.lq;
@@ -331,8 +334,9 @@ __device__ __forceinline__ UnitInfo decode_item(int it, const int32_t* __restric
                                                 const int32_t* __restrict__ cu_k, int kn,
                                                 int split_start, int num_units,
                                                 const int32_t* __restrict__ tail_prefix,
-                                                bool causal) {
-  if (it < split_start) return decode_unit(it, order, prefix, num_seqs, cu_q, cu_k, kn, causal);
+                                                bool causal, int head_begin) {
+  if (it < split_start)
+    return decode_unit(it, order, prefix, num_seqs, cu_q, cu_k, kn, causal, head_begin);
   const int k = it - split_start;
   int lo = 0, hi = num_units - split_start - 1;
   while (lo < hi) {
@@ -340,7 +344,8 @@ __device__ __forceinline__ UnitInfo decode_item(int it, const int32_t* __restric
     if (__ldg(tail_prefix + mid) <= k) lo = mid; else hi = mid - 1;
   }
   // (split units are never causal: the plan does not split under the mask)
-  UnitInfo ui = decode_unit(split_start + lo, order, prefix, num_seqs, cu_q, cu_k, kn, causal);
+  UnitInfo ui =
+      decode_unit(split_start + lo, order, prefix, num_seqs, cu_q, cu_k, kn, causal, head_begin);
   const int c0 = __ldg(tail_prefix + lo);
   const int chunks = __ldg(tail_prefix + lo + 1) - c0;
   if (chunks > 1) {
@@ -813,7 +818,8 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       if (u >= num_items) break;
       if (leader) pending = atomicAdd(p.status + kHdrNextItem, 1);
       const UnitInfo ui = decode_item(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, G::KN,
-                                        split_start, num_units, tail_prefix, p.causal != 0);
+                                        split_start, num_units, tail_prefix, p.causal != 0,
+                                        p.head_begin);
       if (ui.nkv == 0) continue;
       // maps of this sequence: box A of q, k, v, then box B of q, k, v
       const uint8_t* mq = p.ws + L.maps + (size_t)ui.seq * kMapsPerSeq * kMapBytes;
@@ -967,7 +973,8 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       const int u = next_item(k);
       if (u < 0 || u >= num_items) break;
       const UnitInfo ui = decode_item(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, G::KN,
-                                        split_start, num_units, tail_prefix, p.causal != 0);
+                                        split_start, num_units, tail_prefix, p.causal != 0,
+                                        p.head_begin);
       if (ui.nkv == 0) continue;
       if (!(ok = wait_(bar(G::B_Q_FULL), q_use & 1u))) break;
       ++q_use;
@@ -1125,7 +1132,8 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       const int u = next_item(k);
       if (u < 0 || u >= num_items) break;
       const UnitInfo ui = decode_item(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, KN,
-                                        split_start, num_units, tail_prefix, p.causal != 0);
+                                        split_start, num_units, tail_prefix, p.causal != 0,
+                                        p.head_begin);
       if (t == 1 && !ui.t1) continue;
       const int row = ui.q0 + kBlockM * t + r;
       const bool valid = row < ui.lq;
