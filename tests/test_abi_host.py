@@ -71,10 +71,10 @@ P = 0x100000  # a fake, 16-byte aligned address; never dereferenced
     ((P, P, P, P, P, -1, 4, 72, P, None), B.ERR_INVALID_ARG),
     # num_heads < 1
     ((P, P, P, P, P, 1, 0, 72, P, None), B.ERR_INVALID_ARG),
-    # head_dim not one of 64, 72, 80, 96, 128
+    # head_dim not one of 64, 72, 80, 96, 128, 256
     ((P, P, P, P, P, 1, 4, 48, P, None), B.ERR_UNSUPPORTED_DIM),
     ((P, P, P, P, P, 1, 4, 100, P, None), B.ERR_UNSUPPORTED_DIM),
-    ((P, P, P, P, P, 1, 4, 256, P, None), B.ERR_UNSUPPORTED_DIM),
+    ((P, P, P, P, P, 1, 4, 192, P, None), B.ERR_UNSUPPORTED_DIM),
     # null pointers
     ((None, P, P, P, P, 1, 4, 72, P, None), B.ERR_INVALID_ARG),
     ((P, P, P, P, None, 1, 4, 128, P, None), B.ERR_INVALID_ARG),

@@ -61,7 +61,7 @@ def _brute_force(q, k, v, cu_q, cu_k, H, D, causal=False):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D", [4, 72, 128])
+@pytest.mark.parametrize("D", [4, 72, 128, 256])
 def test_brute_force_tiny(D, causal):
     rng = np.random.default_rng(30 + D)
     from oracle_pins import _cu, _rand_bits

@@ -35,6 +35,10 @@ SMALL = [
     ((5, 130, 0, 257, 1, 64), None, 3, 80), ((100, 300, 7), (257, 64, 1000), 2, 80),
     ((1,), None, 2, 96), ((200,), (95,), 2, 96), ((129,), (97,), 2, 96), ((300,), (193,), 1, 96),
     ((5, 130, 0, 257, 1, 64), None, 3, 96), ((100, 300, 7), (257, 64, 1000), 2, 96),
+    # head_dim 256 (its own kernel: 64-key tiles, the two Q tiles of a unit in turn)
+    ((1,), None, 2, 256), ((200,), (63,), 2, 256), ((129,), (65,), 2, 256),
+    ((128,), (128,), 1, 256), ((300,), (1000,), 1, 256), ((5, 130, 0, 257, 1, 64), None, 3, 256),
+    ((100, 300, 7), (257, 64, 1000), 2, 256), ((10, 5, 3), (0, 7, 0), 2, 256),
 ]
 
 
@@ -219,7 +223,7 @@ def _scale_keys(x, scale_of_key):
     return x
 
 
-@pytest.mark.parametrize("D", [72, 128])
+@pytest.mark.parametrize("D", [72, 128, 256])
 def test_running_max_rises_every_tile(cuda_lib, D):
     """Key norms step up every 128 keys, so a row's running max rises by more
     than the rescale threshold at tile starts: the O/l rescale runs."""
@@ -228,7 +232,7 @@ def test_running_max_rises_every_tile(cuda_lib, D):
     check_full(cuda_lib, w, x=x, short_sequences=True)
 
 
-@pytest.mark.parametrize("D", [72, 128])
+@pytest.mark.parametrize("D", [72, 128, 256])
 def test_running_max_rises_in_second_half(cuda_lib, D):
     """Only the second 64 keys of each tile step up, so the first half's P is
     computed against the old max and must be rescaled with O and l."""
@@ -237,7 +241,7 @@ def test_running_max_rises_in_second_half(cuda_lib, D):
     check_full(cuda_lib, w, x=x, short_sequences=True)
 
 
-@pytest.mark.parametrize("D", [72, 128])
+@pytest.mark.parametrize("D", [72, 128, 256])
 def test_running_max_huge_jump(cuda_lib, D):
     """A jump far beyond the exp2 range of the old max (scores x60 from key
     300 on): no overflow leaks into the result."""
@@ -324,7 +328,7 @@ def test_tail_split_mixed_batch(cuda_lib):
                  bound=bf16_bound(ref[live], absv[live]))
 
 
-@pytest.mark.parametrize("D", [64, 80, 96])
+@pytest.mark.parametrize("D", [64, 80, 96, 256])
 def test_other_head_dims_sampled(cuda_lib, D):
     """A longer sequence at every extra head_dim: 512 rows per head."""
     w = Workload(f"L4500_H8_D{D}", (4500,), 8, D, seed=50 + D)
@@ -341,6 +345,7 @@ CAUSAL = [
     ((100, 7), (257, 1000), 2, 72), ((300,), (1000,), 2, 128), ((300,), (100,), 2, 72),
     ((257,), (5,), 2, 128), ((400, 3), (0, 3), 2, 72), ((300,), None, 2, 96),
     ((200, 31), (250, 600), 2, 80), ((640,), (113,), 1, 72), ((129,), (1,), 2, 64),
+    ((300,), None, 2, 256), ((100, 7), (257, 1000), 2, 256), ((300,), (100,), 2, 256),
 ]
 
 

@@ -26,7 +26,8 @@ VARIANTS = {
     "testhooks": ("libattn_varlen_testhooks.so",
                  ["-DATTN_VARLEN_WAIT_LIMIT_NS=50000000ull", "-DATTN_VARLEN_TEST_HOOKS=1"]),
 }
-SOURCES = ["attn_varlen_api.cu", "attn_varlen_kernels.cu", "paged_decode.cu", "chunk_o.cu"]
+SOURCES = ["attn_varlen_api.cu", "attn_varlen_kernels.cu", "attn_varlen_d256.cu",
+           "paged_decode.cu", "chunk_o.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
               "-I", INCLUDE, "-I", CSRC]

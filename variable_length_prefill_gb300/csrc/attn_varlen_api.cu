@@ -286,7 +286,7 @@ static int fwd_owned(const void* q, const void* k, const void* v, const int32_t*
   if ((rc = get_encoder())) return rc;
   // the library-owned workspace also holds the tail-split region (one item
   // per CTA of the persistent grid)
-  const int cap = st.sm_count;
+  const int cap = avp::tail_split_supported(head_dim) ? st.sm_count : 0;
   if ((rc = ensure_workspace(st, avp::ws_layout(num_seqs).total + avp::split_layout(cap).total)))
     return rc;
   return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, st.ws, cap,
@@ -498,7 +498,7 @@ const char* attn_varlen_strerror(int code) {
   switch (code) {
     case ATTN_VARLEN_OK: return "ok";
     case ATTN_VARLEN_ERR_INVALID_ARG: return "invalid argument";
-    case ATTN_VARLEN_ERR_UNSUPPORTED_DIM: return "head_dim must be 64, 72, 80, 96 or 128";
+    case ATTN_VARLEN_ERR_UNSUPPORTED_DIM: return "head_dim must be 64, 72, 80, 96, 128 or 256";
     case ATTN_VARLEN_ERR_MISALIGNED: return "q, k, v and out must be 16-byte aligned (cu_seqlens 4-byte)";
     case ATTN_VARLEN_ERR_UNSUPPORTED_DEVICE: return "current device is not sm_103 (GB300)";
     case ATTN_VARLEN_ERR_CUDA: return "CUDA runtime error";

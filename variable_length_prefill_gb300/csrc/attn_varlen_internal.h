@@ -128,9 +128,15 @@ struct FwdParams {
   int test_withhold; // read only by test builds (ATTN_VARLEN_TEST_HOOKS); 0 otherwise
 };
 
-// Kernel launchers (attn_varlen_kernels.cu).
+// Kernel launchers (attn_varlen_kernels.cu; head_dim 256: attn_varlen_d256.cu).
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
-bool head_dim_supported(int head_dim);  // 64, 72, 80, 96, 128
+bool head_dim_supported(int head_dim);  // 64, 72, 80, 96, 128, 256
+bool tail_split_supported(int head_dim);  // units may be split along keys
+cudaError_t prepare_fwd_d256();
+cudaError_t launch_fwd_d256(const FwdParams& p, int grid, cudaStream_t stream);
+int fwd_threads_d256();
+size_t fwd_smem_bytes_d256();
+int kv_tile_rows_d256();
 cudaError_t prepare_fwd(int head_dim);  // per device and head_dim, before the first launch
 cudaError_t launch_fwd(int head_dim, const FwdParams& p, int grid, cudaStream_t stream);
 int fwd_threads(int head_dim);

@@ -63,6 +63,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "attn_varlen_device.cuh"
 #include "attn_varlen_internal.h"
 #include "ptx.cuh"
 
@@ -70,9 +71,7 @@ namespace avp {
 
 namespace {
 
-constexpr int kItemDepth = 4; // work items handed from the producer to the other roles
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;
 // S(j+1) of a tile overwrites the TMEM columns that P(j) of the same tile
 // occupies.  tcgen05.mma operations issued by one thread execute in issue
 // order, so S(j+1) is queued right behind P(j).V(j); with kStrictPvWait the
@@ -81,12 +80,6 @@ constexpr float kRescaleThreshold = 8.0f;
 #define ATTN_VARLEN_STRICT_PV_WAIT 0
 #endif
 constexpr bool kStrictPvWait = ATTN_VARLEN_STRICT_PV_WAIT != 0;
-// Time after which a wait gives up.  The product build waits 4 s; a test
-// build shortens it to run the give-up path (see ATTN_VARLEN_TEST_HOOKS).
-#ifndef ATTN_VARLEN_WAIT_LIMIT_NS
-#define ATTN_VARLEN_WAIT_LIMIT_NS 4000000000ull
-#endif
-constexpr uint64_t kWaitLimitNs = ATTN_VARLEN_WAIT_LIMIT_NS;
 // Test builds only (never the product library): with FwdParams::test_withhold
 // set, CTA 0's producer neither issues nor announces its first K/V tile, so
 // the MMA warp's wait on that slot runs out and the give-up path (status
@@ -269,129 +262,6 @@ struct Geometry {
   __host__ __device__ static constexpr uint32_t o_col(int t) { return PSEP ? 2u * KN + 128u + DP * t : 256u + 128u * t; }
   static_assert(o_col(1) + DP <= 512, "TMEM columns");
 };
-
-struct UnitInfo {
-  int seq, head, q0, lq, lk, qbase;
-  int jb, nkv;     // this item's key tiles: [jb, jb + nkv) (Q tile 1, or 0 alone)
-  int nkv0;        // key tiles Q tile 0 needs (< nkv only with the causal mask)
-  int coff;        // causal mask: row r sees keys <= r + coff (coff = L_k - L_q)
-  int chunks;      // items the unit is split into (1: not split)
-  int part, part0, tail;  // split items: partial slot, the unit's first slot, tail unit
-  bool t1;  // second Q tile holds at least one row
-};
-
-// Unit u -> sequence, head (offset by head_begin: the call may cover a
-// sub-range of the tensors' heads), 256-row block and key-tile range.
-__device__ __forceinline__ UnitInfo decode_unit(int u, const int32_t* __restrict__ order,
-                                                const int32_t* __restrict__ prefix, int num_seqs,
-                                                const int32_t* __restrict__ cu_q,
-                                                const int32_t* __restrict__ cu_k, int kn,
-                                                bool causal, int head_begin) {
-  // largest rank r in [0, num_seqs) with prefix[r] <= u
-  int lo = 0, hi = num_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(prefix + mid) <= u) lo = mid; else hi = mid - 1;
-  }
-  UnitInfo ui;
-  ui.seq = __ldg(order + lo);
-  const int local = u - __ldg(prefix + lo);
-  ui.qbase = __ldg(cu_q + ui.seq);
-  ui.lq = __ldg(cu_q + ui.seq + 1) - ui.qbase;
-  const int kb = __ldg(cu_k + ui.seq);
-  ui.lk = __ldg(cu_k + ui.seq + 1) - kb;
-  if (ui.lk < 0) ui.lk = 0;
-  const int pairs = (ui.lq + kUnitRows - 1) / kUnitRows;
-  const int hl = local / pairs;
-  ui.head = head_begin + hl;
-  const int qb = local - hl * pairs;
-  // causal: the last row blocks see the most keys, so they go first
-  ui.q0 = (causal ? pairs - 1 - qb : qb) * kUnitRows;
-  ui.t1 = ui.q0 + kBlockM < ui.lq;
-  ui.nkv = (ui.lk + kn - 1) / kn;
-  ui.nkv0 = ui.nkv;
-  ui.coff = ui.lk - ui.lq;
-  if (causal) {
-    // keys visible to the last row of each tile: min(L_k, row + 1 + coff)
-    const int last1 = min(ui.q0 + kUnitRows, ui.lq) - 1;
-    const int last0 = min(ui.q0 + kBlockM, ui.lq) - 1;
-    const int k1 = max(0, min(ui.lk, last1 + 1 + ui.coff));
-    const int k0 = max(0, min(ui.lk, last0 + 1 + ui.coff));
-    ui.nkv = (k1 + kn - 1) / kn;
-    ui.nkv0 = (k0 + kn - 1) / kn;
-  }
-  ui.jb = 0;
-  ui.chunks = 1;
-  ui.part = ui.part0 = ui.tail = -1;
-  return ui;
-}
-
-// Work item -> unit and key-tile range.  Items below split_start are whole
-// units; the others are chunks of the tail units (tail_prefix).
-__device__ __forceinline__ UnitInfo decode_item(int it, const int32_t* __restrict__ order,
-                                                const int32_t* __restrict__ prefix, int num_seqs,
-                                                const int32_t* __restrict__ cu_q,
-                                                const int32_t* __restrict__ cu_k, int kn,
-                                                int split_start, int num_units,
-                                                const int32_t* __restrict__ tail_prefix,
-                                                bool causal, int head_begin) {
-  if (it < split_start)
-    return decode_unit(it, order, prefix, num_seqs, cu_q, cu_k, kn, causal, head_begin);
-  const int k = it - split_start;
-  int lo = 0, hi = num_units - split_start - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(tail_prefix + mid) <= k) lo = mid; else hi = mid - 1;
-  }
-  // (split units are never causal: the plan does not split under the mask)
-  UnitInfo ui =
-      decode_unit(split_start + lo, order, prefix, num_seqs, cu_q, cu_k, kn, causal, head_begin);
-  const int c0 = __ldg(tail_prefix + lo);
-  const int chunks = __ldg(tail_prefix + lo + 1) - c0;
-  if (chunks > 1) {
-    const int c = k - c0;
-    const int jb = (int)(((long long)c * ui.nkv) / chunks);
-    const int je = (int)(((long long)(c + 1) * ui.nkv) / chunks);
-    ui.jb = jb;
-    ui.nkv = je - jb;
-    ui.nkv0 = ui.nkv;
-    ui.chunks = chunks;
-    ui.part = k;
-    ui.part0 = c0;
-    ui.tail = lo;
-  }
-  return ui;
-}
-
-// Bounded wait: spins on the barrier, gives up after kWaitLimitNs or as soon
-// as another role of the CTA has given up.  Returns false on give-up.
-__device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity,
-                                               volatile int* abort_flag, int* status, int code) {
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(status, code);
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             int* status, int code) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait_bounded_slow(bar, parity, abort_flag, status, code);
-}
-
-// Wait with a fixed bound and no abort check (used only while draining).
-__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > kWaitLimitNs) return;
-}
 
 // The i-th K/V tile a unit with n key tiles puts into the ring, in the order
 // the MMA warp first uses them.  Returns true for a V tile; j = key tile.
@@ -1369,11 +1239,15 @@ static auto with_head_dim(int head_dim, F&& f) -> decltype(f(std::integral_const
 }
 
 bool head_dim_supported(int head_dim) {
-  return head_dim == 64 || head_dim == 72 || head_dim == 80 || head_dim == 96 || head_dim == 128;
+  return head_dim == 64 || head_dim == 72 || head_dim == 80 || head_dim == 96 ||
+         head_dim == 128 || head_dim == 256;
 }
 
+// head_dim 256 runs its own kernel (attn_varlen_d256.cu); every other
+// supported head_dim an instance of attn_varlen_fwd_kernel.
 cudaError_t prepare_fwd(int head_dim) {
   if (!head_dim_supported(head_dim)) return cudaErrorInvalidValue;
+  if (head_dim == 256) return prepare_fwd_d256();
   return with_head_dim(head_dim, [](auto d) {
     constexpr int D = decltype(d)::value;
     return cudaFuncSetAttribute(attn_varlen_fwd_kernel<D>,
@@ -1384,27 +1258,33 @@ cudaError_t prepare_fwd(int head_dim) {
 
 cudaError_t launch_fwd(int head_dim, const FwdParams& p, int grid, cudaStream_t stream) {
   if (!head_dim_supported(head_dim)) return cudaErrorInvalidValue;
+  if (head_dim == 256) return launch_fwd_d256(p, grid, stream);
   return with_head_dim(head_dim, [&](auto d) { return launch_fwd_t<decltype(d)::value>(p, grid, stream); });
 }
 
 int fwd_threads(int head_dim) {
+  if (head_dim == 256) return fwd_threads_d256();
   return with_head_dim(head_dim, [](auto d) { return Geometry<decltype(d)::value>::THREADS; });
 }
 
 size_t fwd_smem_bytes(int head_dim) {
+  if (head_dim == 256) return fwd_smem_bytes_d256();
   return with_head_dim(head_dim,
                        [](auto d) { return (size_t)Geometry<decltype(d)::value>::SMEM_BYTES; });
 }
 
 int box_cols(int head_dim) {
+  if (head_dim == 256) return 64;
   return with_head_dim(head_dim, [](auto d) { return Cfg<decltype(d)::value>::BW; });
 }
 
 int kv_tile_rows(int head_dim) {
+  if (head_dim == 256) return kv_tile_rows_d256();
   return with_head_dim(head_dim, [](auto d) { return Cfg<decltype(d)::value>::KN; });
 }
 
 int box_b_cols(int head_dim) {
+  if (head_dim == 256) return 64;  // four 64-column boxes of the box-A map
   return with_head_dim(head_dim, [](auto d) {
     using G = Geometry<decltype(d)::value>;
     return G::NB == 1 ? G::BW : G::WB;  // one box: box B is never loaded
@@ -1412,7 +1292,10 @@ int box_b_cols(int head_dim) {
 }
 
 bool box_b_swizzle_128(int head_dim) {
+  if (head_dim == 256) return true;
   return with_head_dim(head_dim, [](auto d) { return !Geometry<decltype(d)::value>::ZB; });
 }
+
+bool tail_split_supported(int head_dim) { return head_dim != 256; }
 
 }  // namespace avp
