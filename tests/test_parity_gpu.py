@@ -37,7 +37,8 @@ SMALL = [
     ((5, 130, 0, 257, 1, 64), None, 3, 96), ((100, 300, 7), (257, 64, 1000), 2, 96),
     # head_dim 256 (its own kernel: 64-key tiles, the two Q tiles of a unit in turn)
     ((1,), None, 2, 256), ((200,), (63,), 2, 256), ((129,), (65,), 2, 256),
-    ((128,), (128,), 1, 256), ((300,), (1000,), 1, 256), ((5, 130, 0, 257, 1, 64), None, 3, 256),
+    ((128,), (128,), 1, 256), ((256,), (192,), 2, 256), ((64,), (256,), 1, 256),
+    ((300,), (1000,), 1, 256), ((5, 130, 0, 257, 1, 64), None, 3, 256),
     ((100, 300, 7), (257, 64, 1000), 2, 256), ((10, 5, 3), (0, 7, 0), 2, 256),
 ]
 

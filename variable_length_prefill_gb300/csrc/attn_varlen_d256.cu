@@ -425,6 +425,14 @@ __global__ void __launch_bounds__(d256::THREADS, 1)
             pk[c] = pack_bf16x2(a.x, a.y);
             pk[c + 1] = pack_bf16x2(b.x, b.y);
           }
+          // Observe the completion of P(j-1).V(j-1) before P(j) is handed
+          // over: every PV_DONE phase is then waited for in order, so a
+          // parity wait can never match a phase two completions old (the
+          // epilogue's and the rescale's waits rely on it).
+          if (j > 0) {
+            if (!(ok = wait_(bar(B_PV_DONE), (p_cnt - 1) & 1u))) break;
+            tc_fence_after();
+          }
           tmem_st32(tS, pk);
           tmem_wait_st();
           l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
