@@ -22,7 +22,18 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// The tensor-map templates of the last call on a device: encoding them is
+// pure host work that depends only on the buffers and the shape, so a call
+// with the same q, k, v, num_heads and head_dim reuses them.
+struct TemplateCache {
+  const void* bases[3] = {nullptr, nullptr, nullptr};
+  int num_heads = 0;
+  int head_dim = 0;
+  CUtensorMap tmpl[2][6];
+};
+
 struct DeviceState {
+  TemplateCache tc;
   bool probed = false;
   bool supported = false;
   bool prepared[129] = {};  // kernel attributes set, by head_dim
@@ -165,9 +176,22 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const 
   avp::PlanParams pp;
   std::memset(&pp, 0, sizeof(pp));
   const void* bases[avp::kTensors] = {q, k, v};
-  if (avp::encode_templates(reinterpret_cast<avp::EncodeTiledFn>(g_encode), pp, bases, num_heads,
-                            head_dim) != 0)
-    return ATTN_VARLEN_ERR_DRIVER;
+  TemplateCache& tc = st.tc;
+  static_assert(sizeof(tc.tmpl) == sizeof(pp.tmpl), "template cache");
+  if (tc.bases[0] == q && tc.bases[1] == k && tc.bases[2] == v && tc.num_heads == num_heads &&
+      tc.head_dim == head_dim) {
+    std::memcpy(pp.tmpl, tc.tmpl, sizeof(pp.tmpl));
+  } else {
+    if (avp::encode_templates(reinterpret_cast<avp::EncodeTiledFn>(g_encode), pp, bases,
+                              num_heads, head_dim) != 0)
+      return ATTN_VARLEN_ERR_DRIVER;
+    std::memcpy(tc.tmpl, pp.tmpl, sizeof(pp.tmpl));
+    tc.bases[0] = q;
+    tc.bases[1] = k;
+    tc.bases[2] = v;
+    tc.num_heads = num_heads;
+    tc.head_dim = head_dim;
+  }
   for (int m = 0; m < avp::kTensors; ++m) pp.base[m] = static_cast<const uint8_t*>(bases[m]);
   pp.cu_q = cu_q;
   pp.cu_k = cu_k;
@@ -407,6 +431,7 @@ int paged_attn_decode(const void* query, const void* k_cache, const void* v_cach
   p.head_size = head_size;
   p.max_blocks = max_blocks_per_seq;
   p.num_blocks = num_blocks;
+  p.sm_count = st.sm_count;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_size));
   return map_cuda(avp::launch_paged_decode(p, dtype == PAGED_ATTN_FP16, stream));
 }

@@ -1204,8 +1204,11 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------- launch
+// A small batch plans in one warp or eight (fewer threads to launch and to
+// synchronise); the kernel's loops take any multiple of 32 threads.
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
-  attn_varlen_plan_kernel<<<1, 1024, 0, stream>>>(p);
+  const int threads = p.num_seqs <= 32 ? 32 : (p.num_seqs <= 256 ? 256 : 1024);
+  attn_varlen_plan_kernel<<<1, threads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

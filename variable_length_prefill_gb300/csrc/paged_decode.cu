@@ -98,13 +98,42 @@ __global__ void __launch_bounds__(32 * kWarps) paged_decode_kernel(const __grid_
     for (int i = threadIdx.x; i < nq * D; i += blockDim.x) out[i] = from_f32<T>(0.f);
     return;
   }
+  const int tok = lane & 15, half = lane >> 4;
+  const int nblk = (L + kBlock - 1) / kBlock;
+  const int32_t* table = p.block_tables + (size_t)seq * p.max_blocks;
+  // One block's keys (this lane's token, half of the dimensions) and values
+  // (this lane's dimensions, 16 tokens) in registers.  A block id outside
+  // [0, num_blocks) is never dereferenced: it is reported and skipped.
+  uint4 kc[HCH], vc[2 * DPL];
+  auto load_block = [&](int b) -> bool {
+    if (b < 0 || b >= p.num_blocks) {
+      if (lane == 0) atomicOr(p.status, kPagedStatusBadBlock);
+      return false;
+    }
+    const uint4* kb = reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_cache) +
+                                                     ((size_t)b * p.num_kv_heads + g) * D * kBlock);
+#pragma unroll
+    for (int c = 0; c < HCH; ++c) kc[c] = __ldg(kb + (half * HCH + c) * kBlock + tok);
+    const T* vb = static_cast<const T*>(p.v_cache) + ((size_t)b * p.num_kv_heads + g) * D * kBlock +
+                  (size_t)lane * DPL * kBlock;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) {
+      vc[2 * e] = __ldg(reinterpret_cast<const uint4*>(vb + e * kBlock));
+      vc[2 * e + 1] = __ldg(reinterpret_cast<const uint4*>(vb + e * kBlock) + 1);
+    }
+    return true;
+  };
+  // The warp's first block is read before the query is staged, so its memory
+  // round trip overlaps the query's; later blocks are read one iteration
+  // ahead of their use, their ids one further.
+  bool have = warp < nblk ? load_block(__ldg(table + warp)) : false;
+  int b_next = warp + kWarps < nblk ? __ldg(table + warp + kWarps) : 0;
   for (int i = threadIdx.x; i < MQ * D; i += blockDim.x) {
     const int hh = i / D, d = i % D;
     s_q[hh][d + (d >= D / 2 ? 4 : 0)] = hh < nq ? to_f32<T>(q[i]) * p.scale_log2 : 0.f;
   }
   __syncthreads();
 
-  const int tok = lane & 15, half = lane >> 4;
   float m[MQ], l[MQ], o[MQ][DPL];
 #pragma unroll
   for (int hh = 0; hh < MQ; ++hh) {
@@ -113,33 +142,18 @@ __global__ void __launch_bounds__(32 * kWarps) paged_decode_kernel(const __grid_
 #pragma unroll
     for (int e = 0; e < DPL; ++e) o[hh][e] = 0.f;
   }
-  const int nblk = (L + kBlock - 1) / kBlock;
-  const int32_t* table = p.block_tables + (size_t)seq * p.max_blocks;
-  int b_next = warp < nblk ? __ldg(table + warp) : 0;
   for (int jb = warp; jb < nblk; jb += kWarps) {
-    const int b = b_next;
-    if (jb + kWarps < nblk) b_next = __ldg(table + jb + kWarps);  // next block's id, early
-    if (b < 0 || b >= p.num_blocks) {  // never dereference a bad block id
-      if (lane == 0) atomicOr(p.status, kPagedStatusBadBlock);
+    if (!have) {  // this block's id was bad: fetch the next one and go on
+      if (jb + kWarps < nblk) {
+        have = load_block(b_next);
+        if (jb + 2 * kWarps < nblk) b_next = __ldg(table + jb + 2 * kWarps);
+      }
       continue;
     }
     // scores of this lane's token for every query head (half the dimensions)
-    const uint4* kb = reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_cache) +
-                                                     ((size_t)b * p.num_kv_heads + g) * D * kBlock);
     float acc[MQ];
 #pragma unroll
     for (int hh = 0; hh < MQ; ++hh) acc[hh] = 0.f;
-    uint4 kc[HCH];
-#pragma unroll
-    for (int c = 0; c < HCH; ++c) kc[c] = __ldg(kb + (half * HCH + c) * kBlock + tok);
-    const T* vb = static_cast<const T*>(p.v_cache) + ((size_t)b * p.num_kv_heads + g) * D * kBlock +
-                  (size_t)lane * DPL * kBlock;
-    uint4 vc[2 * DPL];  // this lane's value rows, in flight with the keys
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) {
-      vc[2 * e] = __ldg(reinterpret_cast<const uint4*>(vb + e * kBlock));
-      vc[2 * e + 1] = __ldg(reinterpret_cast<const uint4*>(vb + e * kBlock) + 1);
-    }
 #pragma unroll
     for (int c = 0; c < HCH; ++c) {
       float kf[8];
@@ -193,6 +207,12 @@ __global__ void __launch_bounds__(32 * kWarps) paged_decode_kernel(const __grid_
       }
     }
     __syncwarp();
+    // the warp's next block: its keys and values into the same registers
+    have = false;
+    if (jb + kWarps < nblk) {
+      have = load_block(b_next);
+      if (jb + 2 * kWarps < nblk) b_next = __ldg(table + jb + 2 * kWarps);
+    }
   }
 
   // merge the warps: O = sum_w 2^(m_w - m*) O_w, l likewise
@@ -236,12 +256,17 @@ cudaError_t launch_mq(const PagedParams& p, cudaStream_t stream) {
 }
 
 // The head group is the smallest power of two (at most kMaxQ) covering the
-// query heads of one KV head.
+// query heads of one KV head, halved while the grid would not fill the SMs:
+// a smaller group gives more CTAs (each KV block is then read by several,
+// mostly from L2) and shorter per-block work for the few that run.
 template <int D, typename T>
 cudaError_t launch_t(const PagedParams& p, cudaStream_t stream) {
-  if (p.qpk <= 1) return launch_mq<D, T, 1>(p, stream);
-  if (p.qpk <= 2) return launch_mq<D, T, 2>(p, stream);
-  if (p.qpk <= 4) return launch_mq<D, T, 4>(p, stream);
+  int mq = p.qpk <= 1 ? 1 : (p.qpk <= 2 ? 2 : (p.qpk <= 4 ? 4 : kMaxQ));
+  const long long pairs = (long long)p.num_seqs * p.num_kv_heads;
+  while (mq > 1 && pairs * ((p.qpk + mq - 1) / mq) < p.sm_count) mq >>= 1;
+  if (mq == 1) return launch_mq<D, T, 1>(p, stream);
+  if (mq == 2) return launch_mq<D, T, 2>(p, stream);
+  if (mq == 4) return launch_mq<D, T, 4>(p, stream);
   return launch_mq<D, T, kMaxQ>(p, stream);
 }
 

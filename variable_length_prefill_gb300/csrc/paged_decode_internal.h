@@ -27,6 +27,7 @@ struct PagedParams {
   int head_size;
   int max_blocks;
   int num_blocks;
+  int sm_count;               // SMs of the device (sizes the head group)
   float scale_log2;           // head_size^-1/2 * log2(e)
 };
 
