@@ -48,11 +48,11 @@ NOMINAL_BF16_TFLOPS = 2250.0  # GB300 dense bf16, nominal (context; the roofline
 GRAPH_CALLS = 20              # calls per CUDA-graph replay for the launch-bound workload
 
 
-# The sources that build, plan and launch attn_varlen_fwd_kernel (the paged
+# The sources that build, plan and launch the attention kernels (the paged
 # decode and chunked delta-rule kernels live in translation units of their own
-# and cannot change it).
+# and cannot change them).
 ATTN_KERNEL_SOURCES = ("attn_varlen_api.cu", "attn_varlen_internal.h", "attn_varlen_kernels.cu",
-                       "ptx.cuh")
+                       "attn_varlen_device.cuh", "attn_varlen_d256.cu", "ptx.cuh")
 
 
 def kernel_source_sha() -> str:
