@@ -10,36 +10,42 @@
 // ctx_len <= 0 gets a zero row.
 //
 // The operation is a gather-GEMV: every context byte is read once and each
-// (block, KV head) holds 4 KB of contiguous K (D = 128) and 4 KB of V, so the
-// kernel is bound by HBM (or, for the page's small shapes, by latency).  It
-// uses plain coalesced 16-byte loads, no tensor cores:
-//   CTA  = (sequence, KV head, group of up to MQ query heads), 4 warps, MQ
-//          the power of two (at most 8) that covers the query heads per KV
-//          head, so registers scale with the group;
-//   warp = every 4th block of the context, an exp2 online softmax per head;
-//   keys:   lane = (token 0-15, half of the head dimension): 16-byte chunks
-//           [c][token][8] of one half are 256 contiguous bytes per warp load,
-//           the two halves' partial dot products meet by one shuffle;
-//   values: lane = D/32 consecutive dimensions, each a 32-byte row of the
-//           block's 16 tokens;
-//   the four warps' (m, l, O) merge through shared memory at the end.
-// A block's value rows are loaded together with its key chunks, and each
-// warp reads its next block-table entry before working on the current block,
-// so a block costs one dependent memory round trip.
+// (block, KV head) holds D x 16 contiguous keys and D x 16 contiguous values
+// (4 KB each for D = 128), so the kernel is bound by HBM, or for the page's
+// small shapes by latency.  No tensor cores:
+//   grid  = persistent CTAs, each walking (sequence, KV head, group of up to
+//           MQ query heads) pairs with a stride of gridDim.x; MQ is the power
+//           of two (at most 8) that covers the query heads per KV head,
+//           halved while the pairs would not fill the SMs;
+//   warp 4 (producer) streams each block's keys and values with two
+//           cp.async.bulk copies into a ring of stages, across pair
+//           boundaries, so many blocks are in flight per SM;
+//   warps 0-3 (consumers) take the blocks round-robin (block i of the CTA's
+//           stream goes to warp i mod 4, stage i mod STAGES), each with an
+//           exp2 online softmax per head; keys: lane = (token, half of the
+//           dimensions), one shuffle to add the halves; values: lane = the
+//           dimensions lane, lane + 32, ...; per pair the four warps' (m, l,
+//           O) merge through shared memory.
+// Every wait is bounded like the attention kernels'.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
+#include "attn_varlen_device.cuh"
 #include "paged_decode_internal.h"
+#include "ptx.cuh"
 
 namespace avp {
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kConsumers = 4;                    // consumer warps
+constexpr int kThreads = 32 * (kConsumers + 1);  // + the producer warp
 constexpr int kBlock = 16;   // tokens per cache block
 constexpr int kMaxQ = 8;     // query heads per CTA at most
+constexpr int kMaxDevices = 64;
 
 template <typename T>
 __device__ __forceinline__ float to_f32(T x);
@@ -63,195 +69,276 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   for (int i = 0; i < 8; ++i) f[i] = to_f32<T>(e[i]);
 }
 
-__device__ __forceinline__ float fast_ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
+// Shared-memory layout of one kernel instance.
+template <int D, int MQ>
+struct PagedSmem {
+  static constexpr uint32_t KV_BYTES = D * kBlock * 2;    // one block's keys (or values)
+  static constexpr uint32_t STAGE = 2 * KV_BYTES;          // keys, then values
+  static constexpr int STAGES = D == 256 ? 4 : 8;           // a multiple of kConsumers
+  static_assert(STAGES % kConsumers == 0, "stage i mod STAGES belongs to warp i mod 4");
+  static constexpr int QROW = D + 4;  // second half of a query row 4 floats on
+  static constexpr uint32_t RING_OFF = 0;
+  static constexpr uint32_t Q_OFF = RING_OFF + STAGES * STAGE;
+  static constexpr uint32_t P_OFF = Q_OFF + MQ * QROW * 4;
+  static constexpr uint32_t M_OFF = P_OFF + kConsumers * MQ * kBlock * 4;
+  static constexpr uint32_t L_OFF = M_OFF + kConsumers * MQ * 4;
+  static constexpr uint32_t O_OFF = L_OFF + kConsumers * MQ * 4;
+  static constexpr uint32_t BAR_OFF = (O_OFF + kConsumers * MQ * D * 4 + 7u) & ~7u;
+  static constexpr uint32_t OK_OFF = BAR_OFF + 2 * STAGES * 8;  // int per stage: block id valid
+  static constexpr uint32_t ABORT_OFF = OK_OFF + STAGES * 4;
+  static constexpr uint32_t BYTES = ABORT_OFF + 16 + 128;       // + alignment slack
+};
 
 template <int D, typename T, int MQ>
-__global__ void __launch_bounds__(32 * kWarps) paged_decode_kernel(const __grid_constant__ PagedParams p) {
+__global__ void __launch_bounds__(kThreads) paged_decode_kernel(const __grid_constant__ PagedParams p) {
+  using S = PagedSmem<D, MQ>;
   constexpr int NCH = D / 8;        // 16-byte chunks of a key row
   constexpr int HCH = NCH / 2;      // chunks per lane (one half of the row)
   constexpr int DPL = D / 32;       // value dimensions per lane
-  // query row: the second half of the dimensions sits 4 floats further on, so
-  // the two half-warps' broadcast reads fall in different banks
-  constexpr int QROW = D + 4;
-  __shared__ __align__(16) float s_q[MQ][QROW];   // scaled queries
-  __shared__ float s_p[kWarps][MQ][kBlock];       // one block's weights per warp
-  __shared__ float s_m[kWarps][MQ], s_l[kWarps][MQ];
-  __shared__ float s_o[kWarps][MQ][D];
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 127u) & ~127u;
+  uint8_t* bp = smem_raw + (base - raw);
+  float (*s_q)[S::QROW] = reinterpret_cast<float (*)[S::QROW]>(bp + S::Q_OFF);
+  float (*s_p)[MQ][kBlock] = reinterpret_cast<float (*)[MQ][kBlock]>(bp + S::P_OFF);
+  float (*s_m)[MQ] = reinterpret_cast<float (*)[MQ]>(bp + S::M_OFF);
+  float (*s_l)[MQ] = reinterpret_cast<float (*)[MQ]>(bp + S::L_OFF);
+  float (*s_o)[MQ][D] = reinterpret_cast<float (*)[MQ][D]>(bp + S::O_OFF);
+  volatile int* blk_ok = reinterpret_cast<volatile int*>(bp + S::OK_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bp + S::ABORT_OFF);
+  auto full = [&](int s) -> uint32_t { return base + S::BAR_OFF + 8u * (uint32_t)s; };
+  auto empty = [&](int s) -> uint32_t { return base + S::BAR_OFF + 8u * (uint32_t)(S::STAGES + s); };
 
-  const int ngroups = (p.qpk + MQ - 1) / MQ;
-  const int seq = blockIdx.x / (p.num_kv_heads * ngroups);
-  const int rem = blockIdx.x - seq * p.num_kv_heads * ngroups;
-  const int g = rem / ngroups;
-  const int h0 = g * p.qpk + (rem - g * ngroups) * MQ;   // first query head of the CTA
-  const int nq = min(MQ, g * p.qpk + p.qpk - h0);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const T* q = static_cast<const T*>(p.query) + ((size_t)seq * p.num_query_heads + h0) * D;
-  T* out = static_cast<T*>(p.out) + ((size_t)seq * p.num_query_heads + h0) * D;
-
-  int L = p.seq_lens[seq];
-  if (L > p.max_blocks * kBlock) L = p.max_blocks * kBlock;  // the table holds no more
-  if (L <= 0) {
-    for (int i = threadIdx.x; i < nq * D; i += blockDim.x) out[i] = from_f32<T>(0.f);
-    return;
-  }
-  const int tok = lane & 15, half = lane >> 4;
-  const int nblk = (L + kBlock - 1) / kBlock;
-  const int32_t* table = p.block_tables + (size_t)seq * p.max_blocks;
-  // One block's keys (this lane's token, half of the dimensions) and values
-  // (this lane's dimensions, 16 tokens) in registers.  A block id outside
-  // [0, num_blocks) is never dereferenced: it is reported and skipped.
-  uint4 kc[HCH], vc[2 * DPL];
-  auto load_block = [&](int b) -> bool {
-    if (b < 0 || b >= p.num_blocks) {
-      if (lane == 0) atomicOr(p.status, kPagedStatusBadBlock);
-      return false;
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
     }
-    const uint4* kb = reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_cache) +
-                                                     ((size_t)b * p.num_kv_heads + g) * D * kBlock);
-#pragma unroll
-    for (int c = 0; c < HCH; ++c) kc[c] = __ldg(kb + (half * HCH + c) * kBlock + tok);
-    const T* vb = static_cast<const T*>(p.v_cache) + ((size_t)b * p.num_kv_heads + g) * D * kBlock +
-                  (size_t)lane * DPL * kBlock;
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) {
-      vc[2 * e] = __ldg(reinterpret_cast<const uint4*>(vb + e * kBlock));
-      vc[2 * e + 1] = __ldg(reinterpret_cast<const uint4*>(vb + e * kBlock) + 1);
-    }
-    return true;
-  };
-  // The warp's first block is read before the query is staged, so its memory
-  // round trip overlaps the query's; later blocks are read one iteration
-  // ahead of their use, their ids one further.
-  bool have = warp < nblk ? load_block(__ldg(table + warp)) : false;
-  int b_next = warp + kWarps < nblk ? __ldg(table + warp + kWarps) : 0;
-  for (int i = threadIdx.x; i < MQ * D; i += blockDim.x) {
-    const int hh = i / D, d = i % D;
-    s_q[hh][d + (d >= D / 2 ? 4 : 0)] = hh < nq ? to_f32<T>(q[i]) * p.scale_log2 : 0.f;
+    *abort_flag = 0;
+    fence_mbar_init();
   }
   __syncthreads();
 
-  float m[MQ], l[MQ], o[MQ][DPL];
-#pragma unroll
-  for (int hh = 0; hh < MQ; ++hh) {
-    m[hh] = -INFINITY;
-    l[hh] = 0.f;
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) o[hh][e] = 0.f;
-  }
-  for (int jb = warp; jb < nblk; jb += kWarps) {
-    if (!have) {  // this block's id was bad: fetch the next one and go on
-      if (jb + kWarps < nblk) {
-        have = load_block(b_next);
-        if (jb + 2 * kWarps < nblk) b_next = __ldg(table + jb + 2 * kWarps);
-      }
-      continue;
-    }
-    // scores of this lane's token for every query head (half the dimensions)
-    float acc[MQ];
-#pragma unroll
-    for (int hh = 0; hh < MQ; ++hh) acc[hh] = 0.f;
-#pragma unroll
-    for (int c = 0; c < HCH; ++c) {
-      float kf[8];
-      unpack8<T>(kc[c], kf);
-      const int d0 = (half * HCH + c) * 8 + half * 4;  // padded query row
-#pragma unroll
-      for (int hh = 0; hh < MQ; ++hh) {
-        if (hh < nq) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[hh] = fmaf(s_q[hh][d0 + e], kf[e], acc[hh]);
+  const int ngroups = (p.qpk + MQ - 1) / MQ;
+  const int pairs = p.num_seqs * p.num_kv_heads * ngroups;
+  // pair -> sequence, KV head, first query head, query heads, blocks
+  auto decode = [&](int pr, int& seq, int& g, int& h0, int& nq, int& nblk) {
+    seq = pr / (p.num_kv_heads * ngroups);
+    const int rem = pr - seq * p.num_kv_heads * ngroups;
+    g = rem / ngroups;
+    h0 = g * p.qpk + (rem - g * ngroups) * MQ;
+    nq = min(MQ, g * p.qpk + p.qpk - h0);
+    int L = p.seq_lens[seq];
+    if (L > p.max_blocks * kBlock) L = p.max_blocks * kBlock;  // the table holds no more
+    nblk = L > 0 ? (L + kBlock - 1) / kBlock : 0;
+    return L;
+  };
+
+  if (warp == kConsumers) {
+    // ------------------------------------------------------------ producer
+    uint32_t item = 0;
+    bool ok = true;
+    for (int pr = blockIdx.x; ok && pr < pairs; pr += gridDim.x) {
+      int seq, g, h0, nq, nblk;
+      decode(pr, seq, g, h0, nq, nblk);
+      const int32_t* table = p.block_tables + (size_t)seq * p.max_blocks;
+      for (int jb = 0; jb < nblk; ++jb, ++item) {
+        const int s = item % S::STAGES;
+        const uint32_t use = item / S::STAGES;
+        const bool w = wait_bounded(empty(s), (use & 1u) ^ 1u, abort_flag, p.status,
+                                    kStatusTimeoutLoad);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        if (lane == 0) {
+          const int b = __ldg(table + jb);
+          if (b < 0 || b >= p.num_blocks) {  // never dereference a bad block id
+            atomicOr(p.status, kPagedStatusBadBlock);
+            blk_ok[s] = 0;
+            mbar_arrive(full(s));
+          } else {
+            blk_ok[s] = 1;
+            const size_t off = ((size_t)b * p.num_kv_heads + g) * D * kBlock;
+            const uint32_t dst = base + S::RING_OFF + (uint32_t)s * S::STAGE;
+            mbar_arrive_expect_tx(full(s), S::STAGE);
+            bulk_copy_g2s(dst, static_cast<const T*>(p.k_cache) + off, S::KV_BYTES, full(s));
+            bulk_copy_g2s(dst + S::KV_BYTES, static_cast<const T*>(p.v_cache) + off, S::KV_BYTES,
+                          full(s));
+          }
         }
+        __syncwarp();
       }
     }
-    const bool live = jb * kBlock + tok < L;
+    if (!ok) {
+      // let every copy already issued land before the CTA can exit
+      const uint32_t first = item > (uint32_t)S::STAGES ? item - S::STAGES : 0;
+      for (uint32_t it = first; it < item; ++it) wait_drain(full(it % S::STAGES), (it / S::STAGES) & 1u);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  // Control flow is the same in every consumer warp (the named barrier below
+  // counts all four); a warp whose wait gave up only skips its arithmetic.
+  const int tok = lane & 15, half = lane >> 4;
+  bool ok = true;
+  uint32_t item = 0;
+  for (int pr = blockIdx.x; pr < pairs; pr += gridDim.x) {
+    int seq, g, h0, nq, nblk;
+    const int L = decode(pr, seq, g, h0, nq, nblk);
+    const T* q = static_cast<const T*>(p.query) + ((size_t)seq * p.num_query_heads + h0) * D;
+    T* out = static_cast<T*>(p.out) + ((size_t)seq * p.num_query_heads + h0) * D;
+    named_bar_sync(1, 32 * kConsumers);  // the previous pair's merge has read shared memory
+    for (int i = threadIdx.x; i < MQ * D; i += 32 * kConsumers) {
+      const int hh = i / D, d = i % D;
+      s_q[hh][d + (d >= D / 2 ? 4 : 0)] = hh < nq ? to_f32<T>(q[i]) * p.scale_log2 : 0.f;
+    }
+    named_bar_sync(1, 32 * kConsumers);
+    float m[MQ], l[MQ], o[MQ][DPL];
 #pragma unroll
     for (int hh = 0; hh < MQ; ++hh) {
-      if (hh >= nq) continue;
-      float sc = acc[hh] + __shfl_xor_sync(0xffffffffu, acc[hh], 16);
-      sc = live ? sc : -INFINITY;
-      float bm = sc;
+      m[hh] = -INFINITY;
+      l[hh] = 0.f;
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
-      const float mn = fmaxf(m[hh], bm);  // finite: every block holds a live token
-      const float alpha = fast_ex2(m[hh] - mn);
-      const float pw = fast_ex2(sc - mn);
-      float bs = pw;
-#pragma unroll
-      for (int off = 8; off > 0; off >>= 1) bs += __shfl_xor_sync(0xffffffffu, bs, off);
-      l[hh] = l[hh] * alpha + bs;
-      m[hh] = mn;
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) o[hh][e] *= alpha;
-      if (half == 0) s_p[warp][hh][tok] = pw;
+      for (int e = 0; e < DPL; ++e) o[hh][e] = 0.f;
     }
-    __syncwarp();
-    // values: this lane's DPL dimensions, 16 tokens each
+    // this warp's blocks: stream items item + jb with (item + jb) mod 4 == warp
+    const int jb0 = (warp - (int)(item % kConsumers) + kConsumers) % kConsumers;
+    for (int jb = jb0; jb < nblk; jb += kConsumers) {
+      const uint32_t it = item + (uint32_t)jb;
+      const int s = it % S::STAGES;
+      if (ok) {
+        const bool w = wait_bounded(full(s), (it / S::STAGES) & 1u, abort_flag, p.status,
+                                    kStatusTimeoutSoftmax);
+        ok = __all_sync(0xffffffffu, w);
+      }
+      if (!ok || !blk_ok[s]) {
+        __syncwarp();
+        if (lane == 0 && ok) mbar_arrive(empty(s));
+        continue;
+      }
+      const uint8_t* stage = bp + S::RING_OFF + (size_t)s * S::STAGE;
+      // scores of this lane's token for every query head (half the dimensions)
+      const uint4* kb = reinterpret_cast<const uint4*>(stage);
+      float acc[MQ];
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) {
-      float v0[8], v1[8];
-      unpack8<T>(vc[2 * e], v0);
-      unpack8<T>(vc[2 * e + 1], v1);
+      for (int hh = 0; hh < MQ; ++hh) acc[hh] = 0.f;
+#pragma unroll
+      for (int c = 0; c < HCH; ++c) {
+        float kf[8];
+        unpack8<T>(kb[(half * HCH + c) * kBlock + tok], kf);
+        const int d0 = (half * HCH + c) * 8 + half * 4;  // padded query row
+#pragma unroll
+        for (int hh = 0; hh < MQ; ++hh) {
+          if (hh < nq) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[hh] = fmaf(s_q[hh][d0 + e], kf[e], acc[hh]);
+          }
+        }
+      }
+      const bool live = jb * kBlock + tok < L;
 #pragma unroll
       for (int hh = 0; hh < MQ; ++hh) {
         if (hh >= nq) continue;
-        float a = o[hh][e];
+        float sc = acc[hh] + __shfl_xor_sync(0xffffffffu, acc[hh], 16);
+        sc = live ? sc : -INFINITY;
+        float bm = sc;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) a = fmaf(s_p[warp][hh][t], v0[t], a);
+        for (int off = 8; off > 0; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+        const float mn = fmaxf(m[hh], bm);  // finite: every block holds a live token
+        const float alpha = ex2(m[hh] - mn);
+        const float pw = ex2(sc - mn);
+        float bs = pw;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) a = fmaf(s_p[warp][hh][8 + t], v1[t], a);
-        o[hh][e] = a;
+        for (int off = 8; off > 0; off >>= 1) bs += __shfl_xor_sync(0xffffffffu, bs, off);
+        l[hh] = l[hh] * alpha + bs;
+        m[hh] = mn;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[hh][e] *= alpha;
+        if (half == 0) s_p[warp][hh][tok] = pw;
+      }
+      __syncwarp();
+      // values: dimensions lane, lane + 32, ...; 16 tokens each (32 bytes)
+      const uint4* vb = reinterpret_cast<const uint4*>(stage + S::KV_BYTES);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) {
+        float v0[8], v1[8];
+        const int d = e * 32 + lane;
+        unpack8<T>(vb[2 * d], v0);
+        unpack8<T>(vb[2 * d + 1], v1);
+#pragma unroll
+        for (int hh = 0; hh < MQ; ++hh) {
+          if (hh >= nq) continue;
+          float a = o[hh][e];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) a = fmaf(s_p[warp][hh][t], v0[t], a);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) a = fmaf(s_p[warp][hh][8 + t], v1[t], a);
+          o[hh][e] = a;
+        }
+      }
+      // the stage's shared-memory reads come before its next bulk copy
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(s));
+    }
+    item += (uint32_t)nblk;
+
+    // merge the warps: O = sum_w 2^(m_w - m*) O_w, l likewise
+    if (lane == 0) {
+#pragma unroll
+      for (int hh = 0; hh < MQ; ++hh) {
+        s_m[warp][hh] = m[hh];
+        s_l[warp][hh] = l[hh];
       }
     }
-    __syncwarp();
-    // the warp's next block: its keys and values into the same registers
-    have = false;
-    if (jb + kWarps < nblk) {
-      have = load_block(b_next);
-      if (jb + 2 * kWarps < nblk) b_next = __ldg(table + jb + 2 * kWarps);
+#pragma unroll
+    for (int hh = 0; hh < MQ; ++hh)
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) s_o[warp][hh][e * 32 + lane] = o[hh][e];
+    named_bar_sync(1, 32 * kConsumers);
+    for (int i = threadIdx.x; i < nq * D; i += 32 * kConsumers) {
+      const int hh = i / D, d = i % D;
+      float mm = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) mm = fmaxf(mm, s_m[w][hh]);
+      float num = 0.f, den = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) {
+        if (s_m[w][hh] == -INFINITY) continue;  // a warp that saw no block
+        const float f = ex2(s_m[w][hh] - mm);
+        num += f * s_o[w][hh][d];
+        den += f * s_l[w][hh];
+      }
+      out[i] = from_f32<T>(den > 0.f ? num / den : 0.f);
     }
-  }
-
-  // merge the warps: O = sum_w 2^(m_w - m*) O_w, l likewise
-  if (lane == 0) {
-#pragma unroll
-    for (int hh = 0; hh < MQ; ++hh) {
-      s_m[warp][hh] = m[hh];
-      s_l[warp][hh] = l[hh];
-    }
-  }
-#pragma unroll
-  for (int hh = 0; hh < MQ; ++hh)
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) s_o[warp][hh][lane * DPL + e] = o[hh][e];
-  __syncthreads();
-  for (int i = threadIdx.x; i < nq * D; i += blockDim.x) {
-    const int hh = i / D, d = i % D;
-    float mm = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, s_m[w][hh]);
-    float num = 0.f, den = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      if (s_m[w][hh] == -INFINITY) continue;  // a warp that saw no block
-      const float f = fast_ex2(s_m[w][hh] - mm);
-      num += f * s_o[w][hh][d];
-      den += f * s_l[w][hh];
-    }
-    out[i] = from_f32<T>(den > 0.f ? num / den : 0.f);
   }
 }
 
 template <int D, typename T, int MQ>
 cudaError_t launch_mq(const PagedParams& p, cudaStream_t stream) {
   const int ngroups = (p.qpk + MQ - 1) / MQ;
-  const long long grid = (long long)p.num_seqs * p.num_kv_heads * ngroups;
-  if (grid <= 0) return cudaSuccess;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  paged_decode_kernel<D, T, MQ><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
+  const long long pairs = (long long)p.num_seqs * p.num_kv_heads * ngroups;
+  if (pairs <= 0) return cudaSuccess;
+  if (pairs > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  using S = PagedSmem<D, MQ>;
+  auto kern = paged_decode_kernel<D, T, MQ>;
+  // per device: the shared-memory opt-in and the resident CTAs per SM
+  static int resident[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (resident[dev] == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::BYTES);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, S::BYTES);
+    if (e != cudaSuccess) return e;
+    resident[dev] = n > 0 ? n : 1;
+  }
+  const long long grid = std::min<long long>(pairs, (long long)p.sm_count * resident[dev]);
+  kern<<<(unsigned)grid, kThreads, S::BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
