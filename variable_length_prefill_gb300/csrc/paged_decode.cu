@@ -138,27 +138,52 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const __grid_con
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
+    // The CTA's blocks in stream order, 32 at a time: one coalesced read of
+    // 32 block-table entries per chunk, the next chunk's read (possibly the
+    // next pair's) issued before the current chunk's copies, so no copy
+    // waits for its block id.  Pairs with no block add no item.
+    struct Chunk {
+      int pr, seq, g, nblk, jb0;
+    };
+    auto first_from = [&](int pr) -> Chunk {
+      for (; pr < pairs; pr += gridDim.x) {
+        int seq, g, h0, nq, nblk;
+        decode(pr, seq, g, h0, nq, nblk);
+        if (nblk > 0) return Chunk{pr, seq, g, nblk, 0};
+      }
+      return Chunk{pairs, 0, 0, 0, 0};
+    };
+    auto advance = [&](const Chunk& c) -> Chunk {
+      if (c.jb0 + 32 < c.nblk) return Chunk{c.pr, c.seq, c.g, c.nblk, c.jb0 + 32};
+      return first_from(c.pr + (int)gridDim.x);
+    };
+    auto ids_of = [&](const Chunk& c) -> int {
+      if (c.pr >= pairs || c.jb0 + lane >= c.nblk) return 0;
+      return __ldg(p.block_tables + (size_t)c.seq * p.max_blocks + c.jb0 + lane);
+    };
     uint32_t item = 0;
     bool ok = true;
-    for (int pr = blockIdx.x; ok && pr < pairs; pr += gridDim.x) {
-      int seq, g, h0, nq, nblk;
-      decode(pr, seq, g, h0, nq, nblk);
-      const int32_t* table = p.block_tables + (size_t)seq * p.max_blocks;
-      for (int jb = 0; jb < nblk; ++jb, ++item) {
+    Chunk cur = first_from(blockIdx.x);
+    int ids = ids_of(cur);
+    while (ok && cur.pr < pairs) {
+      const Chunk nxt = advance(cur);
+      const int ids_next = ids_of(nxt);
+      const int n = min(32, cur.nblk - cur.jb0);
+      for (int j = 0; j < n; ++j, ++item) {
         const int s = item % S::STAGES;
         const uint32_t use = item / S::STAGES;
         const bool w = wait_bounded(empty(s), (use & 1u) ^ 1u, abort_flag, p.status,
                                     kStatusTimeoutLoad);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        const int b = __shfl_sync(0xffffffffu, ids, j);
         if (lane == 0) {
-          const int b = __ldg(table + jb);
           if (b < 0 || b >= p.num_blocks) {  // never dereference a bad block id
             atomicOr(p.status, kPagedStatusBadBlock);
             blk_ok[s] = 0;
             mbar_arrive(full(s));
           } else {
             blk_ok[s] = 1;
-            const size_t off = ((size_t)b * p.num_kv_heads + g) * D * kBlock;
+            const size_t off = ((size_t)b * p.num_kv_heads + cur.g) * D * kBlock;
             const uint32_t dst = base + S::RING_OFF + (uint32_t)s * S::STAGE;
             mbar_arrive_expect_tx(full(s), S::STAGE);
             bulk_copy_g2s(dst, static_cast<const T*>(p.k_cache) + off, S::KV_BYTES, full(s));
@@ -168,6 +193,8 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const __grid_con
         }
         __syncwarp();
       }
+      cur = nxt;
+      ids = ids_next;
     }
     if (!ok) {
       // let every copy already issued land before the CTA can exit
