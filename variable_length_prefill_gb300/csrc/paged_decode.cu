@@ -46,6 +46,11 @@ constexpr int kThreads = 32 * (kConsumers + 1);  // + the producer warp
 constexpr int kBlock = 16;   // tokens per cache block
 constexpr int kMaxQ = 8;     // query heads per CTA at most
 constexpr int kMaxDevices = 64;
+// Ring stages per CTA (D <= 128; half as many for D = 256): a multiple of
+// the four consumer warps.
+#ifndef ATTN_VARLEN_PAGED_STAGES
+#define ATTN_VARLEN_PAGED_STAGES 8
+#endif
 
 template <typename T>
 __device__ __forceinline__ float to_f32(T x);
@@ -74,7 +79,8 @@ template <int D, int MQ>
 struct PagedSmem {
   static constexpr uint32_t KV_BYTES = D * kBlock * 2;    // one block's keys (or values)
   static constexpr uint32_t STAGE = 2 * KV_BYTES;          // keys, then values
-  static constexpr int STAGES = D == 256 ? 4 : 8;           // a multiple of kConsumers
+  static constexpr int STAGES =
+      D == 256 ? (ATTN_VARLEN_PAGED_STAGES / 2 + 3) / 4 * 4 : ATTN_VARLEN_PAGED_STAGES;
   static_assert(STAGES % kConsumers == 0, "stage i mod STAGES belongs to warp i mod 4");
   static constexpr int QROW = D + 4;  // second half of a query row 4 floats on
   static constexpr uint32_t RING_OFF = 0;
@@ -210,17 +216,35 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const __grid_con
   const int tok = lane & 15, half = lane >> 4;
   bool ok = true;
   uint32_t item = 0;
+  // The query rows of a pair are read one pair ahead into registers (element
+  // threadIdx.x + 128 i of the group's MQ x D), so no pair waits for them.
+  constexpr int QPT = (MQ * D + 32 * kConsumers - 1) / (32 * kConsumers);
+  float qn[QPT];
+  auto load_q = [&](int pr) {
+    int seq, g, h0, nq, nblk;
+    if (pr < pairs) decode(pr, seq, g, h0, nq, nblk);
+#pragma unroll
+    for (int i = 0; i < QPT; ++i) {
+      const int e = threadIdx.x + i * 32 * kConsumers;
+      qn[i] = 0.f;
+      if (pr < pairs && e < MQ * D && e / D < nq)
+        qn[i] = to_f32<T>(static_cast<const T*>(p.query)[((size_t)seq * p.num_query_heads + h0) * D + e]) *
+                p.scale_log2;
+    }
+  };
+  load_q(blockIdx.x);
   for (int pr = blockIdx.x; pr < pairs; pr += gridDim.x) {
     int seq, g, h0, nq, nblk;
     const int L = decode(pr, seq, g, h0, nq, nblk);
-    const T* q = static_cast<const T*>(p.query) + ((size_t)seq * p.num_query_heads + h0) * D;
     T* out = static_cast<T*>(p.out) + ((size_t)seq * p.num_query_heads + h0) * D;
     named_bar_sync(1, 32 * kConsumers);  // the previous pair's merge has read shared memory
-    for (int i = threadIdx.x; i < MQ * D; i += 32 * kConsumers) {
-      const int hh = i / D, d = i % D;
-      s_q[hh][d + (d >= D / 2 ? 4 : 0)] = hh < nq ? to_f32<T>(q[i]) * p.scale_log2 : 0.f;
+#pragma unroll
+    for (int i = 0; i < QPT; ++i) {
+      const int e = threadIdx.x + i * 32 * kConsumers;
+      if (e < MQ * D) s_q[e / D][e % D + (e % D >= D / 2 ? 4 : 0)] = qn[i];
     }
     named_bar_sync(1, 32 * kConsumers);
+    load_q(pr + (int)gridDim.x);  // the next pair's query, in flight during this pair
     float m[MQ], l[MQ], o[MQ][DPL];
 #pragma unroll
     for (int hh = 0; hh < MQ; ++hh) {
@@ -255,18 +279,17 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const __grid_con
         float kf[8];
         unpack8<T>(kb[(half * HCH + c) * kBlock + tok], kf);
         const int d0 = (half * HCH + c) * 8 + half * 4;  // padded query row
+        // every head of the group, also past nq (zero queries, results
+        // unused): branch-free, so the heads' chains interleave
 #pragma unroll
         for (int hh = 0; hh < MQ; ++hh) {
-          if (hh < nq) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[hh] = fmaf(s_q[hh][d0 + e], kf[e], acc[hh]);
-          }
+          for (int e = 0; e < 8; ++e) acc[hh] = fmaf(s_q[hh][d0 + e], kf[e], acc[hh]);
         }
       }
       const bool live = jb * kBlock + tok < L;
 #pragma unroll
       for (int hh = 0; hh < MQ; ++hh) {
-        if (hh >= nq) continue;
         float sc = acc[hh] + __shfl_xor_sync(0xffffffffu, acc[hh], 16);
         sc = live ? sc : -INFINITY;
         float bm = sc;
@@ -295,7 +318,6 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const __grid_con
         unpack8<T>(vb[2 * d + 1], v1);
 #pragma unroll
         for (int hh = 0; hh < MQ; ++hh) {
-          if (hh >= nq) continue;
           float a = o[hh][e];
 #pragma unroll
           for (int t = 0; t < 8; ++t) a = fmaf(s_p[warp][hh][t], v0[t], a);
