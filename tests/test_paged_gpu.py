@@ -53,6 +53,15 @@ EXTRA = [
     PagedWorkload("gqa16", 3, 150, 32, 2, 128, seed=84, shuffle_blocks=True),
     # a long context: each warp walks many blocks
     PagedWorkload("long_ctx", 2, 4100, 8, 1, 128, seed=85, shuffle_blocks=True),
+    # Short tables (at most 8 blocks) with at least four pairs per SM run one
+    # consumer warp per (sequence, KV head, head group) pair: ragged and empty
+    # contexts, head groups of 4 and 2, fp16, head sizes 64 and 256
+    PagedWorkload("wpp_ragged", 700, 100, 4, 1, 128, seed=87, shuffle_blocks=True,
+                  seq_lens=tuple((i * 37) % 106 - 5 for i in range(700))),
+    PagedWorkload("wpp_fp16_g2", 320, 128, 4, 2, 128, dtype="fp16", seed=88, shuffle_blocks=True),
+    PagedWorkload("wpp_d64", 640, 33, 1, 1, 64, seed=89, shuffle_blocks=True,
+                  seq_lens=tuple(33 - i % 34 for i in range(640))),
+    PagedWorkload("wpp_d256", 160, 50, 8, 4, 256, seed=90, shuffle_blocks=True),
 ]
 
 
@@ -78,3 +87,23 @@ def test_bad_block_id_is_reported(cuda_lib):
         _run(cuda_lib, x, w.dtype)
     assert e.value.code == -11
     cuda_lib.check()  # the status word was cleared
+
+
+def test_bad_block_id_warp_per_pair(cuda_lib):
+    """The same check in the warp-per-pair form (short tables, many pairs):
+    the bad block is skipped, every other row still matches the oracle."""
+    from variable_length_prefill_gb300 import AttnVarlenError
+    w = PagedWorkload("bad_wpp", 640, 40, 2, 2, 128, seed=91)
+    x = make_paged_inputs(w)
+    x["block_tables"][5, 1] = -7
+    with pytest.raises(AttnVarlenError) as e:
+        _run(cuda_lib, x, w.dtype)
+    assert e.value.code == -11
+    cuda_lib.check()
+    ok = np.ones(w.num_seqs, dtype=bool)
+    ok[5] = False
+    x2 = {k: (v[ok] if k in ("query", "block_tables", "seq_lens") else v) for k, v in x.items()}
+    got = _run(cuda_lib, x2, w.dtype)
+    ref = oracle.paged_decode(x2["query"], x2["k_cache"], x2["v_cache"], x2["block_tables"],
+                              x2["seq_lens"], w.dtype)
+    assert_close_values(bf16_bits_to_f64(got), ref, w.name)
