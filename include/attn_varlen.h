@@ -170,7 +170,7 @@ int attn_varlen_check_ws(void* workspace, cudaStream_t stream);
  * owns every allocation a plug-in makes, or a latency-critical path where
  * cudaMalloc/cudaFree would synchronise the device.  Instead of the
  * library-owned workspace, it uses one scratch array compiled into the
- * library (about 777 KiB, held on every GPU that loads the library until
+ * library (about 1033 KiB, held on every GPU that loads the library until
  * the process exits), so it supports at most
  * ATTN_VARLEN_NOALLOC_MAX_SEQS sequences per call and returns
  * ATTN_VARLEN_ERR_NOALLOC_LIMIT above that.  Arguments, layout and results

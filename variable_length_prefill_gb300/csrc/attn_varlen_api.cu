@@ -26,10 +26,10 @@ constexpr int kMaxDevices = 64;
 // pure host work that depends only on the buffers and the shape, so a call
 // with the same q, k, v, num_heads and head_dim reuses them.
 struct TemplateCache {
-  const void* bases[3] = {nullptr, nullptr, nullptr};
+  const void* bases[avp::kTensors] = {nullptr, nullptr, nullptr, nullptr};
   int num_heads = 0;
   int head_dim = 0;
-  CUtensorMap tmpl[2][6];
+  CUtensorMap tmpl[2][avp::kMapsPerSeq];
 };
 
 struct DeviceState {
@@ -136,9 +136,10 @@ int encode_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int num_head
 }
 
 // Templates: a 3-D bf16 map {head_dim, num_heads, rows} with box {cols, 1,
-// rows per tile} (128 query rows for q, kv_tile_rows keys for k and v), one
-// for box A (columns [0, 64)) and one for box B (the columns past 64); the
-// plan kernel patches the address and the row extent per sequence.
+// rows per tile} (128 query rows for q, kv_tile_rows keys for k and v,
+// kStoreRows output rows for out), one for box A (columns [0, 64)) and one
+// for box B (the columns past 64); the plan kernel patches the address and
+// the row extent per sequence.
 // Class 0 is encoded one row short of kMapLargeBytes, class 1 at it.
 int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[kTensors],
                      int num_heads, int head_dim) {
@@ -148,7 +149,7 @@ int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[
   for (int m = 0; m < kMapsPerSeq; ++m) {
     const int t = m % kTensors;
     const bool b = m >= kTensors;
-    const int box_rows = t == 0 ? kBlockM : kv_tile_rows(head_dim);
+    const int box_rows = t == 0 ? kBlockM : (t == kOut ? kStoreRows : kv_tile_rows(head_dim));
     const int cols = b ? box_b_cols(head_dim) : box_cols(head_dim);
     const bool swz = b ? box_b_swizzle_128(head_dim) : true;
     for (int cls = 0; cls < 2; ++cls) {
@@ -175,11 +176,11 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const 
   if (head_count < 0) head_count = num_heads;
   avp::PlanParams pp;
   std::memset(&pp, 0, sizeof(pp));
-  const void* bases[avp::kTensors] = {q, k, v};
+  const void* bases[avp::kTensors] = {q, k, v, out};
   TemplateCache& tc = st.tc;
   static_assert(sizeof(tc.tmpl) == sizeof(pp.tmpl), "template cache");
-  if (tc.bases[0] == q && tc.bases[1] == k && tc.bases[2] == v && tc.num_heads == num_heads &&
-      tc.head_dim == head_dim) {
+  if (tc.bases[0] == q && tc.bases[1] == k && tc.bases[2] == v && tc.bases[3] == out &&
+      tc.num_heads == num_heads && tc.head_dim == head_dim) {
     std::memcpy(pp.tmpl, tc.tmpl, sizeof(pp.tmpl));
   } else {
     if (avp::encode_templates(reinterpret_cast<avp::EncodeTiledFn>(g_encode), pp, bases,
@@ -189,6 +190,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const 
     tc.bases[0] = q;
     tc.bases[1] = k;
     tc.bases[2] = v;
+    tc.bases[3] = out;
     tc.num_heads = num_heads;
     tc.head_dim = head_dim;
   }

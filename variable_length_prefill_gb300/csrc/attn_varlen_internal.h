@@ -14,10 +14,14 @@ namespace avp {
 // (128 for head_dim 128, 112 for head_dim 72).
 constexpr int kBlockM = 128;
 constexpr int kUnitRows = 2 * kBlockM;
-constexpr int kTensors = 3;          // q, k, v
-// Tensor maps per sequence: [0, 3) box A of q, k, v (64 columns, 128-byte
-// swizzle), [3, 6) box B of q, k, v (the columns past 64; see box_b_cols)
+constexpr int kTensors = 4;          // q, k, v, out
+constexpr int kOut = 3;              // tensor index of the output
+// Tensor maps per sequence: [0, 4) box A of q, k, v, out (64 columns,
+// 128-byte swizzle), [4, 8) box B of q, k, v, out (the columns past 64; see
+// box_b_cols).  The q, k, v maps load tiles; the out maps store rows from
+// shared memory, kStoreRows rows (one softmax warp's) per box.
 constexpr int kMapsPerSeq = 2 * kTensors;
+constexpr int kStoreRows = 32;
 constexpr int kMapBytes = 128;       // sizeof(CUtensorMap)
 constexpr int kLptMaxSeqs = 2048;    // longest-first ordering up to this many sequences
 
@@ -81,11 +85,11 @@ __host__ __device__ constexpr SplitLayout split_layout(int cap) {
 constexpr uint64_t kMapLargeBytes = 1ull << 17;
 
 struct PlanParams {
-  // host-encoded q/k/v templates: [0] below kMapLargeBytes, [1] at or above
+  // host-encoded q/k/v/out templates: [0] below kMapLargeBytes, [1] at or above
   CUtensorMap tmpl[2][kMapsPerSeq];
   const int32_t* cu_q;
   const int32_t* cu_k;
-  const uint8_t* base[kTensors];  // q, k, v
+  const uint8_t* base[kTensors];  // q, k, v, out
   uint8_t* ws;
   uint8_t* split;  // tail-split region, or null
   int split_cap;   // items the split region holds (0: no tail split)
@@ -107,7 +111,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 // CUresult.
 int encode_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int num_heads, int head_dim,
                uint64_t rows, int box_rows, int box_cols, bool swizzle_128);
-// Fill pp.tmpl for q, k, v at `bases` (both size classes, both boxes).
+// Fill pp.tmpl for q, k, v, out at `bases` (both size classes, both boxes).
 // Returns a CUresult.
 int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[kTensors],
                      int num_heads, int head_dim);

@@ -238,7 +238,17 @@ struct Geometry {
   static constexpr bool LO = ZB && ATTN_VARLEN_SUM_IN_O != 0;
   static constexpr uint32_t ONES_OFF = ZERO_OFF + ZERO_BYTES;
   static constexpr uint32_t ONES_BYTES = LO ? kBlockM * 16u : 0u;
-  static constexpr uint32_t BAR_OFF = ONES_OFF + ONES_BYTES;
+  // Epilogue staging, one region per softmax warp (its 32 output rows): box
+  // A as 32 rows x 128 bytes in the 128-byte swizzle of the out map (1024-
+  // byte aligned), then, for head_dim 72, box B as 32 rows x 16 bytes.  With
+  // a 64-column box B the box-A region is reused once box A's store has read
+  // it.
+  static constexpr uint32_t STG_A_BYTES = kStoreRows * 128u;
+  static constexpr uint32_t STG_B_BYTES = ZB ? kStoreRows * 16u : 0u;
+  static constexpr uint32_t STG_WARP = (STG_A_BYTES + STG_B_BYTES + 1023u) / 1024u * 1024u;
+  static constexpr uint32_t STG_OFF = (ONES_OFF + ONES_BYTES + 1023u) / 1024u * 1024u;
+  static constexpr uint32_t STG_BYTES = SM_WARPS * STG_WARP;
+  static constexpr uint32_t BAR_OFF = STG_OFF + STG_BYTES;
   // barrier slots (8 bytes each)
   static constexpr int B_Q_FULL = 0, B_Q_EMPTY = 1, B_KV_FULL = 2, B_KV_EMPTY = 2 + STAGES,
                        B_S_FULL = 2 + 2 * STAGES, B_P_FULL = B_S_FULL + 2,
@@ -326,15 +336,16 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
       s_key[i] = lq > 0 ? (lk > 0 ? lk : 0) : -1;
     }
   }
-  // one thread per (sequence, map): the q, k and v maps of box A and box B
+  // one thread per (sequence, map): the q, k, v and out maps of box A and box B
   for (int idx = tid; idx < N * kMapsPerSeq; idx += nt) {
     const int i = idx / kMapsPerSeq, m = idx - i * kMapsPerSeq, t = m % kTensors;
     const int q0 = p.cu_q[i], lq = p.cu_q[i + 1] - q0;
     const int k0 = p.cu_k[i], lk = p.cu_k[i + 1] - k0;
     if (lq > 0 && lk > 0) {
       uint8_t* dst = p.ws + L.maps + (size_t)idx * kMapBytes;
-      const int row0 = t == 0 ? q0 : k0;
-      const int len = t == 0 ? lq : lk;
+      const bool qrows = t == 0 || t == kOut;  // q and out: the sequence's query rows
+      const int row0 = qrows ? q0 : k0;
+      const int len = qrows ? lq : lk;
       const int cls = (uint64_t)len * (uint64_t)p.row_bytes >= kMapLargeBytes ? 1 : 0;
       const uint4* src = reinterpret_cast<const uint4*>(&p.tmpl[cls][m]);
       uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -1175,24 +1186,82 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
                         l, orow, valid, ui.part, ui.part0, ui.tail, ui.chunks);
         continue;
       }
+      // TMEM -> registers (O / l, bf16) -> shared memory -> TMA store.  Each
+      // warp stages its 32 rows in the out map's box layout and its lane 0
+      // stores them; rows at or past L_q are outside the map's extent and are
+      // not written.
       const float inv = l > 0.f ? 1.0f / l : 0.f;
+      const int wrow = ui.q0 + kBlockM * t + kStoreRows * qq;  // warp's first row in the sequence
+      const bool any_row = wrow < ui.lq;                        // warp-uniform
+      const int rr = threadIdx.x & 31;                          // row within the box
+      const uint8_t* mo = p.ws + L.maps + ((size_t)ui.seq * kMapsPerSeq + kOut) * kMapBytes;
+      const uint8_t* mob = mo + kTensors * kMapBytes;
+      const uint32_t stg = base + G::STG_OFF + (uint32_t)warp * G::STG_WARP;
+      uint8_t* stg_ptr = base_ptr + G::STG_OFF + (size_t)warp * G::STG_WARP;
+      // the warp's stores of the previous unit have read the staging region
+      if (rr == 0) bulk_wait_read_all();
+      __syncwarp();
+      // 16-byte chunk ch (columns 8 ch .. 8 ch + 7) of this thread's row: box
+      // A (chunks 0-7, 128-byte swizzle), box B after it (head_dim 72, one
+      // unswizzled chunk) or, for a 64-column box B, in box A's region
+      auto put = [&](int ch, uint4 v) {
+        uint32_t off;
+        if (ch < 8)
+          off = (uint32_t)rr * 128u + (uint32_t)((ch ^ (rr & 7)) * 16);
+        else if constexpr (G::ZB)
+          off = G::STG_A_BYTES + (uint32_t)rr * 16u;
+        else
+          off = (uint32_t)rr * 128u + (uint32_t)(((ch - 8) ^ (rr & 7)) * 16);
+        *reinterpret_cast<uint4*>(stg_ptr + off) = v;
+      };
+      auto store_box = [&](const uint8_t* map, int col0) {
+        fence_proxy_async_smem();  // this thread's staging writes, to the async proxy
+        __syncwarp();
+        if (rr == 0 && any_row) {
+          tmap_acquire(map);
+          tma_store_3d(map, stg, col0, ui.head, wrow);
+          bulk_commit();
+        }
+      };
 #pragma unroll
       for (int c = 0; c < G::DP; c += 16) {
+        if (c == 64 && !G::ZB) {
+          // box A's columns are staged: store them, then reuse the region
+          store_box(mo, 0);
+          if (rr == 0) bulk_wait_read_all();
+          __syncwarp();
+        }
         uint32_t o[16];
         tmem_ld16(tO + c, o);
         tmem_wait_ld();
         reg_fence(o, 0, 16);
-        if (valid && c < D) {
+        if (c < D) {
           uint32_t w[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-          uint4* o4 = reinterpret_cast<uint4*>(orow + c);
-          o4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          if (c + 8 < D) o4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          put(c / 8, make_uint4(w[0], w[1], w[2], w[3]));
+          if (c + 8 < D) put(c / 8 + 1, make_uint4(w[4], w[5], w[6], w[7]));
         }
       }
+      if constexpr (G::NB == 1) {
+        store_box(mo, 0);
+      } else if constexpr (G::ZB) {
+        store_box(mo, 0);
+        // box B from its own region
+        if (rr == 0 && any_row) {
+          tmap_acquire(mob);
+          tma_store_3d(mob, stg + G::STG_A_BYTES, G::BW, ui.head, wrow);
+          bulk_commit();
+        }
+      } else {
+        store_box(mob, G::BW);
+      }
+      (void)orow;
+      (void)valid;
     }
+    // every store of this warp has completed before the CTA exits
+    if ((threadIdx.x & 31) == 0) bulk_wait_all();
   }
   __syncwarp();
   tc_fence_before();
