@@ -263,7 +263,7 @@ class L2Flush:
     def __call__(self):
         import torch
         self.w.fill_(1)
-        torch.sum(self.r, dtype=torch.int64, out=self.acc)
+        torch.sum(self.r, dim=0, dtype=torch.int64, out=self.acc)
 
 
 L2_NOTE = "flushed before every step (256 MiB written, then another 256 MiB read)"
