@@ -247,26 +247,32 @@ def whole_job_throughput(job_flops_per_step: float, steps: int, seconds: float) 
 
 
 class L2Flush:
-    """Run before each timed call.  It writes one buffer larger than L2, so
-    every input of the call comes from HBM.  It then reads a second buffer
-    larger than L2, so L2 holds only clean lines and the timed call pays no
-    write-back of the first buffer.  (With the write alone, an HBM-bound call
-    such as paged decode row #0 also wrote up to 129 MB of the flush buffer
-    back to HBM inside its timed region.)"""
+    """Run before each timed call: write a buffer larger than L2, then read
+    it back.  Measured on GB300: after the write alone a 276-token call
+    timed the same as with no flush at all (19.4 against 19.0 us; with the
+    read-back 26.6 us), so the write did not evict a small working set from
+    L2, and it left dirty lines that an HBM-bound call (paged decode row #0:
+    34.8 against 28.7 us) wrote back inside its own timed region.  After
+    the read-back L2 holds clean lines of the buffer only."""
 
     def __init__(self, dev):
         import torch
         self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
         self.acc = torch.zeros((), dtype=torch.int64, device=dev)
 
     def __call__(self):
         import torch
         self.w.fill_(1)
-        torch.sum(self.r, dim=0, dtype=torch.int64, out=self.acc)
+        torch.sum(self.w, dim=0, dtype=torch.int64, out=self.acc)
 
 
-L2_NOTE = "flushed before every step (256 MiB written, then another 256 MiB read)"
+L2_NOTE = "flushed before every step (256 MiB written, then read back)"
+
+
+# GPU-side spin before each timed call (outside the timed region), so the
+# host has queued the call's launches before its start event: a short call
+# is then timed on the device alone, without host enqueue gaps.
+SPIN_CYCLES = 200_000
 
 
 def time_calls(fn, steps, flush_buf, stream):
@@ -275,6 +281,7 @@ def time_calls(fn, steps, flush_buf, stream):
     for _ in range(steps):
         if flush_buf is not None:
             flush_buf()
+        torch.cuda._sleep(SPIN_CYCLES)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)

@@ -1260,8 +1260,9 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       (void)orow;
       (void)valid;
     }
-    // every store of this warp has completed before the CTA exits
-    if ((threadIdx.x & 31) == 0) bulk_wait_all();
+    // every store of this warp has read its staging region before the CTA
+    // exits (the global writes complete on their own)
+    if ((threadIdx.x & 31) == 0) bulk_wait_read_all();
   }
   __syncwarp();
   tc_fence_before();
