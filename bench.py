@@ -348,6 +348,37 @@ def run_profile_chunk(args):
           flush=True)
 
 
+def run_profile_paged(args):
+    """Only paged decode on one of the page's shapes: warm-up and timed calls
+    with L2 flushed before each, for runs under a profiler."""
+    import numpy as np
+    import torch
+
+    import variable_length_prefill_gb300 as vlp
+    dev = torch.device("cuda", 0)
+    vlp.load()
+    pw = PAGED_CONFIGS[args.profile_paged]
+    xs = make_paged_inputs(pw)
+    tdt = torch.bfloat16 if pw.dtype == "bf16" else torch.float16
+    t = {n: torch.from_numpy(xs[n].view(np.int16)).view(tdt).to(dev)
+         for n in ("query", "k_cache", "v_cache")}
+    tables = torch.from_numpy(xs["block_tables"]).to(dev)
+    lens = torch.from_numpy(xs["seq_lens"]).to(dev)
+    out = torch.empty_like(t["query"])
+    flush = L2Flush(dev)
+    fn = lambda: vlp.paged_attn_decode(t["query"], t["k_cache"], t["v_cache"], tables, lens,  # noqa: E731
+                                       out=out)
+    for _ in range(args.warmup):
+        fn()
+    durs = time_calls(fn, args.steps, flush, torch.cuda.current_stream(dev))
+    vlp.check()
+    us = statistics.median(durs) * 1e3
+    print(json.dumps({"profile": True, "workload": "paged_" + pw.name, "steps": args.steps,
+                      "us_median": round(us, 2),
+                      "gbs_algorithmic": round(pw.algorithmic_bytes() / (us * 1e-6) / 1e9, 1)}),
+          flush=True)
+
+
 def workload_config(w, world: int = 1) -> dict:
     """The JSON line's config for workload w (both arms print the same)."""
     return {"workload": w.name, "seq_lens": list(w.seq_lens_q), "num_heads": w.num_heads,
@@ -677,6 +708,8 @@ def main():
                     help="warm-up and timed steps only, for runs under a profiler")
     ap.add_argument("--profile-chunk", choices=sorted(CHUNK_CONFIGS), default=None,
                     help="time only the chunked delta-rule output on this shape (profiler runs)")
+    ap.add_argument("--profile-paged", choices=sorted(PAGED_CONFIGS), default=None,
+                    help="time only paged decode on this shape (profiler runs)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -688,6 +721,9 @@ def main():
         return
     if args.profile_chunk:
         run_profile_chunk(args)
+        return
+    if args.profile_paged:
+        run_profile_paged(args)
         return
     if world > 1:
         import torch.distributed as dist
