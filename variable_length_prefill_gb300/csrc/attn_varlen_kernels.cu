@@ -1023,6 +1023,18 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       // keys this row may see: all L_k, or under the causal mask
       // min(L_k, row + 1 + L_k - L_q) (<= 0: none, the row is zero)
       const int klim = p.causal ? min(ui.lk, row + 1 + ui.coff) : ui.lk;
+      // this sequence's out maps: acquired and prefetched now, so the
+      // epilogue's stores do not wait for their descriptors
+      const uint8_t* mo = p.ws + L.maps + ((size_t)ui.seq * kMapsPerSeq + kOut) * kMapBytes;
+      const uint8_t* mob = mo + kTensors * kMapBytes;
+      if ((threadIdx.x & 31) == 0 && ui.part < 0 && nsteps > 0) {
+        tmap_acquire(mo);
+        tmap_prefetch(mo);
+        if (G::NB == 2) {
+          tmap_acquire(mob);
+          tmap_prefetch(mob);
+        }
+      }
       if (nsteps == 0) {
         if (valid) {
 #pragma unroll
@@ -1194,8 +1206,6 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       const int wrow = ui.q0 + kBlockM * t + kStoreRows * qq;  // warp's first row in the sequence
       const bool any_row = wrow < ui.lq;                        // warp-uniform
       const int rr = threadIdx.x & 31;                          // row within the box
-      const uint8_t* mo = p.ws + L.maps + ((size_t)ui.seq * kMapsPerSeq + kOut) * kMapBytes;
-      const uint8_t* mob = mo + kTensors * kMapBytes;
       const uint32_t stg = base + G::STG_OFF + (uint32_t)warp * G::STG_WARP;
       uint8_t* stg_ptr = base_ptr + G::STG_OFF + (size_t)warp * G::STG_WARP;
       // the warp's stores of the previous unit have read the staging region
@@ -1218,7 +1228,6 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
         fence_proxy_async_smem();  // this thread's staging writes, to the async proxy
         __syncwarp();
         if (rr == 0 && any_row) {
-          tmap_acquire(map);
           tma_store_3d(map, stg, col0, ui.head, wrow);
           bulk_commit();
         }
@@ -1250,7 +1259,6 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
         store_box(mo, 0);
         // box B from its own region
         if (rr == 0 && any_row) {
-          tmap_acquire(mob);
           tma_store_3d(mob, stg + G::STG_A_BYTES, G::BW, ui.head, wrow);
           bulk_commit();
         }
