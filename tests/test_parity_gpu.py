@@ -71,10 +71,14 @@ def test_lk_zero_gives_zero_rows(cuda_lib):
     assert (got[10:15] != 0).any()
 
 
-def test_rows_outside_sequences_untouched(cuda_lib):
+@pytest.mark.parametrize("D", [64, 72, 80, 96, 128, 256])
+def test_rows_outside_sequences_untouched(cuda_lib, D):
     """cu_seqlens starting past row 0, an empty sequence, and rows after the
-    last sequence: a sentinel pattern there must survive bit for bit."""
-    w = Workload("offsets", (40, 0, 200, 3), 2, 128, seed=42, cu_offset=7)
+    last sequence: a sentinel pattern there must survive bit for bit (the
+    epilogue's tiled stores end at each sequence's last row, for every box
+    width: one 64-column box, an 8-column box B, a 64-column box B cut at
+    head_dim)."""
+    w = Workload(f"offsets_{D}", (40, 0, 200, 3), 2, D, seed=42, cu_offset=7)
     x = make_inputs(w)
     # two extra trailing rows beyond cu_q[-1]
     for n in ("q", "k", "v"):
@@ -85,7 +89,7 @@ def test_rows_outside_sequences_untouched(cuda_lib):
     assert (got[:cu[0]] == sentinel).all()
     assert (got[cu[-1]:] == sentinel).all()
     ref = oracle.attn_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"])
-    assert_close(got[cu[0]:cu[-1]], ref[cu[0]:cu[-1]], "offsets")
+    assert_close(got[cu[0]:cu[-1]], ref[cu[0]:cu[-1]], f"offsets D={D}")
 
 
 @pytest.mark.parametrize("D,causal,ws", [(72, False, False), (128, False, True),
@@ -123,7 +127,8 @@ def test_backwards_cu_seqlens(cuda_lib, D, causal, ws):
                  bound=bound)
 
 
-@pytest.mark.parametrize("D,causal", [(72, False), (128, False), (64, True)])
+@pytest.mark.parametrize("D,causal", [(72, False), (128, False), (64, True), (80, False),
+                                     (96, True)])
 def test_head_shards_in_place(cuda_lib, D, causal):
     """attn_varlen_fwd_heads on the shards of a 5-head batch: one shard
     leaves the other heads' rows untouched (a sentinel survives bit for bit),
