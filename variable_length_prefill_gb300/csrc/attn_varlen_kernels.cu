@@ -440,11 +440,23 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
   if (warp == 0) {
     int split_start = U, items = U;
     if (try_split) {
-      int maxn = 0;
-      for (int i = lane; i < R; i += 32) maxn = max(maxn, s_key[i]);
+      int maxn = 0, minn = 0x7fffffff;
+      for (int i = lane; i < R; i += 32) {
+        maxn = max(maxn, s_key[i]);
+        minn = min(minn, s_key[i]);
+      }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) maxn = max(maxn, __shfl_xor_sync(0xffffffffu, maxn, o));
+      for (int o = 16; o > 0; o >>= 1) {
+        maxn = max(maxn, __shfl_xor_sync(0xffffffffu, maxn, o));
+        minn = min(minn, __shfl_xor_sync(0xffffffffu, minn, o));
+      }
       int lo = 1, hi = maxn > 1 ? maxn : 1;
+      if (minn == maxn && maxn > 0) {
+        // equal tail units (every single-sequence call): each may take
+        // grid / R chunks, so the smallest budget is ceil(nkv / (grid / R))
+        const int per = p.grid / R;  // >= 1, as R < grid
+        lo = hi = (maxn + per - 1) / per;
+      }
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
         int sum = 0;
@@ -488,8 +500,10 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
   __syncthreads();
   const int nzero = s_warp[0];
   if (nzero > 0) {
-    int* cnt = reinterpret_cast<int*>(p.split + split_layout(p.split_cap).counters);
-    for (int i = tid; i < nzero * 2 * kBlockM; i += nt) cnt[i] = 0;
+    // 2 x 128 int counters per tail unit, 16 bytes at a time (the region is
+    // 256-byte aligned)
+    uint4* cnt = reinterpret_cast<uint4*>(p.split + split_layout(p.split_cap).counters);
+    for (int i = tid; i < nzero * 2 * kBlockM / 4; i += nt) cnt[i] = make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -1282,10 +1296,11 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------- launch
-// A small batch plans in one warp or eight (fewer threads to launch and to
-// synchronise); the kernel's loops take any multiple of 32 threads.
+// A small batch plans in four warps or eight (fewer threads to launch and to
+// synchronise; four warps still spread the map writes and the zeroing of the
+// tail split's counters); the kernel's loops take any multiple of 32 threads.
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
-  const int threads = p.num_seqs <= 32 ? 32 : (p.num_seqs <= 256 ? 256 : 1024);
+  const int threads = p.num_seqs <= 128 ? 128 : (p.num_seqs <= 256 ? 256 : 1024);
   attn_varlen_plan_kernel<<<1, threads, 0, stream>>>(p);
   return cudaGetLastError();
 }
