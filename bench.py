@@ -35,8 +35,10 @@ if ROOT not in sys.path:
 
 import numpy as np  # noqa: E402
 
-from workloads import (C1, C2, C3, C4, C5, CHUNK_CONFIGS, CONFIGS, PAGED_CONFIGS,  # noqa: E402
-                       make_inputs, make_paged_inputs, sample_rows)
+from workloads import (C1, C2, C3, C4, C5, CHUNK_CONFIGS, CONFIGS, D256, EXTRA_CONFIGS,  # noqa: E402
+                       PAGED_CONFIGS, make_inputs, make_paged_inputs, sample_rows)
+
+ALL_WORKLOADS = {**CONFIGS, **EXTRA_CONFIGS}
 
 HEADLINE = C4
 SECOND = C3  # the other full record (the dense head_dim-128 shape)
@@ -205,7 +207,7 @@ def run_reference(args, rank, world):
     keys each), sized so that warm-up plus timed steps take about a minute."""
     if rank != 0:
         return
-    w = CONFIGS[args.workload] if args.workload else HEADLINE
+    w = ALL_WORKLOADS[args.workload] if args.workload else HEADLINE
     x = make_inputs(w)
     per_step = min(5.0, max(0.2, 60.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
@@ -446,7 +448,7 @@ def run_ours(args, rank, world, local_rank):
         return (f"attn_varlen_fwd_kernel<{w.head_dim}> (+ plan kernel in the timed call)")
 
     flush = L2Flush(dev)
-    w = CONFIGS[args.workload] if args.workload else HEADLINE
+    w = ALL_WORKLOADS[args.workload] if args.workload else HEADLINE
     x, t, cu_q, cu_k = device_inputs(w)
     out = torch.empty_like(t["q"])
     # this rank's heads (all of them on one GPU)
@@ -573,7 +575,7 @@ def run_ours(args, rank, world, local_rank):
                     "roofline": roofline_block(SECOND, tf2, peaks, kernel_name(SECOND)),
                     "clocks": clock_entry(sampler.summary(*win))}
                 del ts, os_
-            for ws in (C1, C2, C3, C4, C5):
+            for ws in (C1, C2, C3, C4, C5, D256):
                 xs, ts, cq, ck = device_inputs(ws)
                 os_ = torch.empty_like(ts["q"])
                 fn = lambda: vlp.attn_varlen_fwd(ts["q"], ts["k"], ts["v"], cq, ck, out=os_)  # noqa: E731
@@ -601,7 +603,7 @@ def run_ours(args, rank, world, local_rank):
                 del ts, os_
             vlp.check()
             # the causal variant of the same workloads (FLOPs of the visible pairs)
-            for ws in (C2, C3, C5):
+            for ws in (C2, C3, C5, D256):
                 xs, ts, cq, ck = device_inputs(ws)
                 os_ = torch.empty_like(ts["q"])
                 fn = lambda: vlp.attn_varlen_fwd(ts["q"], ts["k"], ts["v"], cq, ck, out=os_,  # noqa: E731
@@ -702,7 +704,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--workload", choices=sorted(CONFIGS), default=None,
+    ap.add_argument("--workload", choices=sorted(ALL_WORKLOADS), default=None,
                     help="time this workload instead of the headline one")
     ap.add_argument("--profile", action="store_true",
                     help="warm-up and timed steps only, for runs under a profiler")

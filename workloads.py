@@ -92,6 +92,12 @@ C5 = Workload("C5_packed9_T31673_H4_D72",
 
 CONFIGS = {"C1": C1, "C2": C2, "C3": C3, "C4": C4, "C5": C5}
 
+# head_dim 256 (beyond the page's table, which stops at 128): one long
+# sequence, timed beside the five workloads and profiled on its own.
+D256 = Workload("D256_L16384_H16", (16384,), 16, 256, seed=6,
+                description="one sequence L=16384, H=16, D=256 (head_dim 256)")
+EXTRA_CONFIGS = {"D256": D256}
+
 
 def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """float32 -> bf16 bit patterns (uint16), round to nearest, ties to even."""
