@@ -58,6 +58,18 @@ def test_c5_all_rows(cuda_lib):
     check_full(cuda_lib, C5)
 
 
+def test_c2_all_rows(cuda_lib):
+    """Every output row of C2 (130176 rows of 8136 keys; a few seconds of the
+    oracle on the host cores)."""
+    check_full(cuda_lib, C2)
+
+
+def test_c3_all_rows(cuda_lib):
+    """Every output row of C3 (535744 rows of 16742 keys; about two minutes of
+    the oracle on 16 host cores)."""
+    check_full(cuda_lib, C3)
+
+
 @pytest.mark.parametrize("w,rows", [(C2, 512), (C3, 512), (C4, 512)], ids=lambda x: getattr(x, "name", str(x)))
 def test_full_size_sampled_rows(cuda_lib, w, rows):
     check_sampled(cuda_lib, w, rows)
