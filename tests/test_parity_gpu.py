@@ -326,6 +326,16 @@ def test_tail_split_one_unit_over_the_grid(cuda_lib, D):
     check_rows(cuda_lib, w, rows, x=x, caller_workspace=True)
 
 
+@pytest.mark.parametrize("D", [72, 128])
+def test_tail_split_equal_tail_units(cuda_lib, D):
+    """One sequence of 10000 tokens over 5 heads: 200 units, so on a 152-SM
+    GB300 the last 48 units (equal key ranges) are each cut into
+    floor(152 / 48) = 3 key chunks (the plan's closed-form budget) and
+    merged; every row against the oracle."""
+    w = Workload(f"tail_equal_D{D}", (10000,), 5, D, seed=41 + D)
+    check_full(cuda_lib, w)
+
+
 def test_tail_split_mixed_batch(cuda_lib):
     """Fewer units than SMs, so every unit is in the last partial wave: units
     of 36, 27, 19, 18, 1 and 0 key tiles are cut into different numbers of
