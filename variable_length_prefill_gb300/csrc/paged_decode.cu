@@ -94,6 +94,7 @@ struct PagedSmem {
   static constexpr int STAGES = D == 256 ? (RING / 2 + 3) / 4 * 4 : RING;
   static_assert(STAGES % kConsumers == 0, "stage i mod STAGES belongs to warp i mod 4");
   static constexpr int SPW = STAGES / kConsumers;  // stages of each consumer warp
+  static_assert(SPW >= 1, "every consumer warp owns a stage");
   static constexpr int QROW = D + 4;  // second half of a query row 4 floats on
   static constexpr int QROWS = WPP ? kConsumers * MQ : MQ;  // warp-private rows with WPP
   static constexpr uint32_t RING_OFF = 0;
