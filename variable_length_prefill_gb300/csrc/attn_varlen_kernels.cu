@@ -87,6 +87,12 @@ constexpr bool kStrictPvWait = ATTN_VARLEN_STRICT_PV_WAIT != 0;
 #ifndef ATTN_VARLEN_TEST_HOOKS
 #define ATTN_VARLEN_TEST_HOOKS 0
 #endif
+// The plan kernel is itself a programmatic dependent of the previous
+// attention kernel on the stream: it may be resident before that kernel ends
+// and waits for it (griddepcontrol.wait) before it reads or writes anything.
+#ifndef ATTN_VARLEN_PLAN_PDL
+#define ATTN_VARLEN_PLAN_PDL 1
+#endif
 #ifndef ATTN_VARLEN_TAIL_SPLIT
 #define ATTN_VARLEN_TAIL_SPLIT 1
 #endif
@@ -299,6 +305,11 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
   // the attention kernel may start launching now; it waits for this grid to
   // complete before it reads the workspace
   grid_launch_dependents();
+#if ATTN_VARLEN_PLAN_PDL
+  // the previous attention kernel on the stream (if any) still reads the
+  // workspace: nothing is read or written before it has finished
+  grid_wait_prerequisite();
+#endif
   __shared__ int s_key[kLptMaxSeqs];
   // with at most kLptMaxSeqs sequences the per-sequence lengths, the order
   // and the prefix sums stay in shared memory, so the plan costs one round
@@ -674,6 +685,11 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
 
   // everything above overlaps the plan kernel; the workspace is read below
   grid_wait_prerequisite();
+#if ATTN_VARLEN_PLAN_PDL
+  // the next call's plan kernel may launch now; it waits for this grid to
+  // finish before it touches the workspace
+  grid_launch_dependents();
+#endif
   const WsLayout L = ws_layout(p.num_seqs);
   const int num_units = reinterpret_cast<const int*>(p.ws)[1];
   const int num_items = reinterpret_cast<const int*>(p.ws)[2];
@@ -1301,8 +1317,22 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
 // tail split's counters); the kernel's loops take any multiple of 32 threads.
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
   const int threads = p.num_seqs <= 128 ? 128 : (p.num_seqs <= 256 ? 256 : 1024);
+#if ATTN_VARLEN_PLAN_PDL
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_varlen_plan_kernel, p);
+#else
   attn_varlen_plan_kernel<<<1, threads, 0, stream>>>(p);
   return cudaGetLastError();
+#endif
 }
 
 // Launched as a programmatic dependent of the plan kernel: its CTAs start
