@@ -72,10 +72,14 @@ extern "C" {
  *   stream        CUDA stream the work is queued on (0 = legacy default)
  *
  * Uses a workspace that the library owns, one per device, sized by num_seqs
- * plus a region, sized by the SM count, in which the units of the grid's last
- * partial wave may be split along the key range and merged (fp32 partials,
- * merged in a fixed order, so results are deterministic).  When it must grow,
- * the call synchronises the device once to free the old one.  Calls that share a device must be ordered (same stream, or
+ * plus a region of four times the SM count partial slots (about 135 KB each,
+ * 82 MB on 152 SMs) in which the units at the end of the schedule may be
+ * split along the key range and merged (fp32 partials, merged in a fixed
+ * order, so results are deterministic).  Which units are split is planned on
+ * the device from the lengths: those that a longest-first list schedule of
+ * the persistent grid would finish late.  When the workspace must grow, the
+ * call synchronises the device once to free the old one.  Calls that share a
+ * device must be ordered (same stream, or
  * synchronised); concurrent calls on different streams must each pass their
  * own workspace to attn_varlen_fwd_ws.  Errors detected inside the kernels
  * (a wait that timed out) are recorded in the workspace and reported by

@@ -329,19 +329,21 @@ def test_tail_split_one_unit_over_the_grid(cuda_lib, D):
 @pytest.mark.parametrize("D", [72, 128])
 def test_tail_split_equal_tail_units(cuda_lib, D):
     """One sequence of 10000 tokens over 5 heads: 200 units, so on a 152-SM
-    GB300 the last 48 units (equal key ranges) are each cut into
-    floor(152 / 48) = 3 key chunks (the plan's closed-form budget) and
-    merged; every row against the oracle."""
+    GB300 the second wave's 48 units (equal key ranges) are the late ones and
+    are each cut into floor(152 / 48) = 3 key chunks (the plan's closed-form
+    budget for a short tail of equal units) and merged.  Every row against
+    the oracle."""
     w = Workload(f"tail_equal_D{D}", (10000,), 5, D, seed=41 + D)
     check_full(cuda_lib, w)
 
 
 def test_tail_split_mixed_batch(cuda_lib):
-    """Fewer units than SMs, so every unit is in the last partial wave: units
-    of 36, 27, 19, 18, 1 and 0 key tiles are cut into different numbers of
-    chunks.  Every row against the oracle, through both entry points."""
+    """Fewer units than SMs, so every unit is late in the plan's schedule:
+    units of 81, 54, 45, 19, 1 and 0 key tiles (head_dim 72) are cut into 3,
+    2, 2 and 1 chunks of at most 32 key tiles.  Every row against the oracle,
+    through both entry points."""
     lens_q = (3000, 1, 700, 0, 2048, 5, 300)
-    lens_k = (2000, 4000, 0, 9, 2048, 3000, 1)
+    lens_k = (6000, 9000, 0, 9, 2048, 5000, 1)
     w = Workload("tail_mixed", lens_q, 2, 72, seed=77, seq_lens_k=lens_k)
     x = make_inputs(w)
     check_full(cuda_lib, w, x=x, short_sequences=True)

@@ -19,7 +19,7 @@ import pytest
 
 import oracle
 from gpu_helpers import assert_close, device_inputs, to_bits
-from workloads import C1, make_inputs
+from workloads import C1, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -96,6 +96,37 @@ def test_wait_runs_out_and_is_reported(waitlib, kind):
     assert _run(waitlib, kind, t, cu_q, cu_k, out, s, ws) == 0
     assert _check(waitlib, kind, s, ws) == 0
     assert_close(to_bits(out), ref, f"testhooks build after a timeout, {kind} workspace")
+
+
+def test_split_counters_recover_after_a_timeout(waitlib):
+    """A call whose plan splits units along keys (the library's own
+    workspace) and that times out in CTA 0 can leave the split region's row
+    counters part-counted (a chunk CTA 0 claimed is never run).  The CTA that
+    gave up marks them dirty, and the next call's plan zeroes them: that call
+    must meet the parity bar on every row.  6000 tokens over 7 heads: 168
+    units, the 16 of the second wave cut into 2 key chunks each."""
+    import torch
+    from variable_length_prefill_gb300._binding import ERR_DEVICE_TIMEOUT
+    w = Workload("timeout_split", (6000,), 7, 72, seed=113)
+    x = make_inputs(w)
+    t, cu_q, cu_k = device_inputs(x, "cuda")
+    out = torch.zeros_like(t["q"])
+    ref = oracle.attn_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"])
+    s = ctypes.c_void_p(int(torch.cuda.current_stream().cuda_stream))
+    assert _run(waitlib, "owned", t, cu_q, cu_k, out, s) == 0
+    assert _check(waitlib, "owned", s) == 0
+    assert_close(to_bits(out), ref, "testhooks build, split units")
+    waitlib.attn_varlen_test_withhold(1)
+    try:
+        assert _run(waitlib, "owned", t, cu_q, cu_k, out, s) == 0
+        assert _check(waitlib, "owned", s) == ERR_DEVICE_TIMEOUT
+    finally:
+        waitlib.attn_varlen_test_withhold(0)
+    for _ in range(2):
+        out.zero_()
+        assert _run(waitlib, "owned", t, cu_q, cu_k, out, s) == 0
+        assert _check(waitlib, "owned", s) == 0
+        assert_close(to_bits(out), ref, "testhooks build after a timeout, split units")
 
 
 def test_product_library_has_no_test_hook(cuda_lib):

@@ -165,8 +165,10 @@ int encode_templates(EncodeTiledFn enc, PlanParams& pp, const void* const bases[
 
 namespace {
 
-// `split_cap` > 0: the workspace holds a tail-split region for that many
-// items right after ws_layout(num_seqs).total.  Heads [head_begin,
+// `split_cap` > 0 (library-owned workspace only): the tail-split region for
+// that many items is the last split_layout(split_cap).total bytes of the
+// allocation, so it stays in one place, whatever num_seqs, until the
+// workspace is reallocated (its row counters persist from call to call).  Heads [head_begin,
 // head_begin + head_count) of the num_heads-head tensors are computed
 // (head_count < 0: all of them).
 int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const int32_t* cu_k,
@@ -198,7 +200,9 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_q, const 
   pp.cu_q = cu_q;
   pp.cu_k = cu_k;
   pp.ws = static_cast<uint8_t*>(ws);
-  uint8_t* split = split_cap > 0 ? pp.ws + avp::ws_layout(num_seqs).total : nullptr;
+  uint8_t* split = split_cap > 0 ? static_cast<uint8_t*>(st.ws) + st.ws_bytes -
+                                       avp::split_layout(split_cap).total
+                                 : nullptr;
   pp.split = split;
   pp.split_cap = split_cap;
   pp.grid = st.sm_count;
@@ -256,8 +260,13 @@ int ensure_workspace(DeviceState& st, size_t need) {
     cudaGetLastError();
     return ATTN_VARLEN_ERR_OOM;
   }
+  // header: the carried status word, and the split region's row counters
+  // marked dirty (the first plan zeroes them)
+  int hdr[avp::kHdrCountersDirty + 1] = {};
+  hdr[0] = status;
+  hdr[avp::kHdrCountersDirty] = 1;
   cudaError_t e = cudaMemset(p, 0, 256);
-  if (e == cudaSuccess) e = cudaMemcpy(p, &status, sizeof(int), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(p, hdr, sizeof(hdr), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
     cudaFree(p);
     return fail_cuda(e);
@@ -310,9 +319,9 @@ static int fwd_owned(const void* q, const void* k, const void* v, const int32_t*
   DeviceState& st = g_dev[dev];
   if ((rc = probe_device(dev, st))) return rc;
   if ((rc = get_encoder())) return rc;
-  // the library-owned workspace also holds the tail-split region (one item
-  // per CTA of the persistent grid)
-  const int cap = avp::tail_split_supported(head_dim) ? st.sm_count : 0;
+  // the library-owned workspace also holds the tail-split region
+  // (kSplitWaves items per CTA of the persistent grid)
+  const int cap = avp::tail_split_supported(head_dim) ? avp::kSplitWaves * st.sm_count : 0;
   if ((rc = ensure_workspace(st, avp::ws_layout(num_seqs).total + avp::split_layout(cap).total)))
     return rc;
   return run(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, out, st.ws, cap,

@@ -171,9 +171,16 @@ __global__ void __launch_bounds__(d256::THREADS, 1)
       __syncwarp();
       if (leader) mbar_arrive(bar(B_ITEM_FULL + islot));
       if (u >= num_items) break;
+#if !ATTN_VARLEN_LATE_CLAIM
       if (leader) pending = atomicAdd(p.status + kHdrNextItem, 1);
+#endif
       const UnitInfo ui = decode(u);
-      if (ui.nkv == 0) continue;
+      if (ui.nkv == 0) {
+#if ATTN_VARLEN_LATE_CLAIM
+        if (leader) pending = atomicAdd(p.status + kHdrNextItem, 1);
+#endif
+        continue;
+      }
       const uint8_t* mq = p.ws + L.maps + (size_t)ui.seq * kMapsPerSeq * kMapBytes;
       const uint8_t* mk = mq + kMapBytes;
       const uint8_t* mv = mq + 2 * kMapBytes;
@@ -212,6 +219,10 @@ __global__ void __launch_bounds__(d256::THREADS, 1)
           ++kv_item;
         }
       }
+#if ATTN_VARLEN_LATE_CLAIM
+      // the next item is claimed once this one's last K/V load is out
+      if (leader) pending = atomicAdd(p.status + kHdrNextItem, 1);
+#endif
     }
     if (!ok) {
       // let every copy already issued land before the CTA can exit

@@ -14,6 +14,11 @@ namespace avp {
 namespace {
 
 constexpr int kItemDepth = 4;  // work items handed from the producer to the other roles
+// The producer claims a CTA's next work item once the current item's last
+// K/V load is issued (else: when the current item starts).
+#ifndef ATTN_VARLEN_LATE_CLAIM
+#define ATTN_VARLEN_LATE_CLAIM 1
+#endif
 // Lazy rescale: a row's running max is only raised when the new maximum
 // exceeds it by more than this (log2 units), so exponentials stay <= 2^8.
 constexpr float kRescaleThreshold = 8.0f;

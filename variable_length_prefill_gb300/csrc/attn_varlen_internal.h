@@ -32,9 +32,15 @@ constexpr int kStatusTimeoutSoftmax = 4;
 constexpr int kStatusTimeoutItem = 8;
 // Workspace header word (int32 index) of the dynamic item counter.
 constexpr int kHdrNextItem = 4;
+// Workspace header word: nonzero while the split region's row counters may
+// be nonzero.  Set when the workspace is allocated and by an attention CTA
+// that gave up a wait; the plan kernel then zeroes the counters and clears
+// it (every merge leaves its own counter at zero).
+constexpr int kHdrCountersDirty = 5;
 
 // Workspace: [header 256 B][tensor maps][order int32 N][prefix int32 N+1]
-//   header: int32 status, num_units, num_items, split_start, next_item
+//   header: int32 status, num_units, num_items, split_start, next_item,
+//           counters_dirty
 // Work items: items [0, split_start) are whole units; the units of the last,
 // partial wave, [split_start, num_units), may be split along the key range
 // into several items each (see SplitLayout).
@@ -55,11 +61,16 @@ __host__ __device__ constexpr WsLayout ws_layout(int num_seqs) {
   return w;
 }
 
-// Optional tail-split region (library-owned workspace only), sized for `cap`
-// items = the persistent grid:
+// Optional tail-split region (library-owned workspace only, the last bytes of
+// its allocation, so that its row counters stay in place from call to call),
+// sized for `cap` tail units and items, kSplitWaves times the persistent grid:
 //   tail_prefix int32 [cap + 1]  items per tail unit, prefix-summed
 //   counters    int32 [cap][2][128]  finished chunks per (tail unit, Q tile, row)
 //   partials    f32   [cap][2][kPartRowMax][128]  unnormalised O, m, l (column-major)
+#ifndef ATTN_VARLEN_SPLIT_WAVES
+#define ATTN_VARLEN_SPLIT_WAVES 4
+#endif
+constexpr int kSplitWaves = ATTN_VARLEN_SPLIT_WAVES;
 constexpr int kPartRowMax = 132;  // floats per partial row (head_dim 128: 128 + m + l + pad)
 struct SplitLayout {
   size_t prefix;

@@ -96,9 +96,32 @@ constexpr bool kStrictPvWait = ATTN_VARLEN_STRICT_PV_WAIT != 0;
 #ifndef ATTN_VARLEN_TAIL_SPLIT
 #define ATTN_VARLEN_TAIL_SPLIT 1
 #endif
+// The tail is found by simulating the list schedule (else: the grid's last
+// partial wave).
+#ifndef ATTN_VARLEN_SIM_TAIL
+#define ATTN_VARLEN_SIM_TAIL 1
+#endif
+#ifndef ATTN_VARLEN_MIN_CHUNK
+#define ATTN_VARLEN_MIN_CHUNK 32
+#endif
 // A split pays off only if it shortens the tail by more than the partial
 // write and merge cost, counted in key tiles of work.
 constexpr int kMergeTiles = 8;
+// A chunk of a split unit holds at least this many key tiles (its partial
+// write and the merge cost several).
+constexpr int kMinChunkTiles = ATTN_VARLEN_MIN_CHUNK;
+// A tail with at least this many key tiles per CTA is cut into up to
+// kSplitWaves chunks per CTA; a shorter one into at most one per CTA.
+#ifndef ATTN_VARLEN_FINE_TAIL
+#define ATTN_VARLEN_FINE_TAIL 192
+#endif
+constexpr int kFineTailTiles = ATTN_VARLEN_FINE_TAIL;
+// The plan's model of a unit's cost beyond its key tiles (Q load, epilogue),
+// in key tiles.
+constexpr int kUnitCostTiles = 2;
+// Limits of the plan's list-schedule simulation (steps, CTAs).
+constexpr int kSimMaxSteps = 128;
+constexpr int kSimMaxGrid = 256;
 
 
 // K/V ring depth per head_dim (shared memory: head_dim 72 holds 2 x 18 KB of
@@ -323,6 +346,8 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
   const int N = p.num_seqs;
   const WsLayout L = ws_layout(N);
   int* hdr = reinterpret_cast<int*>(p.ws);
+  // read now, so that the load's latency overlaps the map writes
+  const int counters_dirty = p.split_cap > 0 ? hdr[kHdrCountersDirty] : 0;
   int* order = reinterpret_cast<int*>(p.ws + L.order);
   int* prefix = reinterpret_cast<int*>(p.ws + L.prefix);
   const bool lpt = N <= kLptMaxSeqs;
@@ -426,63 +451,184 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
   }
   __syncthreads();
 
-  // 4. tail split: the units of the last, partial wave of the persistent
-  //    grid are cut along the key range so that the tail fills the grid.
+  // 4. tail split.  The plan first finds where the tail starts: it runs the
+  //    attention kernel's list schedule (units longest first, each to the
+  //    CTA that frees up first; a unit costs its key tiles plus
+  //    kUnitCostTiles) over groups of CTAs that free up at the same time.
+  //    The first unit that would end past 31/32 of the balanced time per
+  //    CTA starts the tail (a unit of the first wave only if it alone runs
+  //    past 33/32 of it); every unit from there on may be cut along the key
+  //    range.  (Without the longest-first order, past kSimMaxSteps steps or
+  //    a grid above kSimMaxGrid, the tail is the grid's last partial wave.)
   //    Chunk count of tail unit i: ceil(nkv_i / T) with the smallest key-tile
-  //    budget T whose total fits the grid.  Everything runs on chip: the
-  //    tail units' key-tile counts go to shared memory (s_key is free now),
-  //    one warp searches T with shuffle reductions.
+  //    budget T (at least kMinChunkTiles) whose total fits the split region.
+  //    Everything runs on chip: the tail units' key-tile counts go to shared
+  //    memory (s_key is free now), one warp simulates (the first rank in
+  //    closed form) and searches T with warp reductions.
   const int U = s_carry;
-  const int R = p.grid > 0 ? U % p.grid : 0;
-  const bool try_split = ATTN_VARLEN_TAIL_SPLIT && !p.causal && p.split_cap >= p.grid &&
-                         p.grid > 0 && R > 0 && R <= kLptMaxSeqs;
-  const int t0 = U - R;  // first tail unit
-  if (try_split) {
-    for (int r = tid; r < N; r += nt) {
-      const int ua = max(prefix_at(r), t0), ub = prefix_at(r + 1);
-      if (ua < ub) {
-        const int lk = lk_of(order_at(r));
-        const int nkv = lk > 0 ? (lk + p.kv_rows - 1) / p.kv_rows : 0;
-        for (int u = ua; u < ub; ++u) s_key[u - t0] = nkv;
+  auto nkv_of = [&](int i) {
+    const int lk = lk_of(i);
+    return lk > 0 ? (lk + p.kv_rows - 1) / p.kv_rows : 0;
+  };
+  __shared__ unsigned s_gt[kSimMaxGrid];   // simulated CTA groups: time they free up
+  __shared__ int s_gc[kSimMaxGrid];        // and their CTA count
+  __shared__ int s_t0;                     // first tail unit (U: none)
+  // (rank 0 holds the most key tiles: if even its units are too short to cut
+  // into two chunks, nothing is split and the schedule is not simulated)
+  const bool try_split = ATTN_VARLEN_TAIL_SPLIT && !p.causal && lpt && p.split_cap >= p.grid &&
+                         p.grid > 0 && U > 0 &&
+                         nkv_of(order_at(0)) > kMinChunkTiles + kMergeTiles;
+  if (warp == 0) {
+    int t0 = U;
+    if (try_split) {
+      t0 = U - U % p.grid;  // the grid's last partial wave
+      if (ATTN_VARLEN_SIM_TAIL && p.grid <= kSimMaxGrid) {
+        long long tot = 0;
+        for (int r = lane; r < N; r += 32) {
+          const int i = order_at(r), k = units_of(i);
+          if (k > 0) tot += (long long)k * (nkv_of(i) + kUnitCostTiles);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        const long long bal = tot / p.grid;
+        const long long late = bal - bal / 32;  // a unit ending past this starts the tail
+        const long long big = bal + bal / 32;   // a first-wave unit this long is late too
+        int found = U;
+        bool done_all = bal < (1ll << 29);  // simulated times fit 32 bits
+        if (done_all) {
+          // rank 0 in closed form (every CTA is free at time 0, so its unit d
+          // starts at (d / grid) n0): the first late wave is the first w >= 1
+          // with (w + 1) n0 > late, or wave 0 for a unit longer than `big`
+          const int k0 = units_of(order_at(0));
+          const long long n0 = nkv_of(order_at(0)) + kUnitCostTiles;
+          const long long w = n0 > big ? 0 : max(1ll, late / n0);
+          if (w * p.grid < k0) {
+            found = (int)(w * p.grid);
+          } else {
+            const int W = k0 / p.grid, rem = k0 - W * p.grid;
+            if (lane == 0) {
+              s_gt[0] = (unsigned)(W * n0);
+              s_gc[0] = p.grid - rem;
+              s_gt[1] = (unsigned)((W + 1) * n0);
+              s_gc[1] = rem;
+            }
+            int ng = rem > 0 ? 2 : 1, steps = 0;
+            __syncwarp();
+            // later ranks step by step, one group of CTAs at a time
+            for (int r = 1; r < N && found == U && done_all; ++r) {
+              const int i = order_at(r), k = units_of(i);
+              const unsigned n = (unsigned)(nkv_of(i) + kUnitCostTiles);
+              for (int d = 0; d < k;) {
+                if (++steps > kSimMaxSteps) {
+                  done_all = false;
+                  break;
+                }
+                // the group that frees up first
+                unsigned mt = 0xffffffffu;
+                int mi = 0;
+                for (int g = lane; g < ng; g += 32)
+                  if (s_gt[g] < mt) {
+                    mt = s_gt[g];
+                    mi = g;
+                  }
+                const unsigned bt = __reduce_min_sync(0xffffffffu, mt);
+                const int src = __ffs(__ballot_sync(0xffffffffu, mt == bt)) - 1;
+                const int bi = __shfl_sync(0xffffffffu, mi, src);
+                // late: it ends past the mark; a unit of the first wave only
+                // if it alone runs longer than `big` (else splitting it
+                // cannot shorten the schedule)
+                if ((long long)bt + n > late && (bt > 0 || n > big)) {
+                  found = prefix_at(r) + d;
+                  break;
+                }
+                const int c = s_gc[bi];
+                const int j = min(k - d, c);
+                __syncwarp();
+                if (lane == 0) {
+                  if (j == c) {
+                    s_gt[bi] = bt + n;
+                  } else {  // j of the group's CTAs take one unit each
+                    s_gc[bi] = c - j;
+                    s_gt[ng] = bt + n;
+                    s_gc[ng] = j;
+                  }
+                }
+                if (j != c) ++ng;
+                __syncwarp();
+                d += j;
+              }
+            }
+          }
+        }
+        if (done_all) t0 = found;
       }
+      // the split region holds at most split_cap tail units (and items)
+      if (U - t0 > p.split_cap) t0 = U - U % p.grid;
     }
+    if (lane == 0) s_t0 = t0;
   }
   __syncthreads();
+  const int t0 = s_t0;  // first tail unit
+  const int R = U - t0;  // tail units
   if (warp == 0) {
     int split_start = U, items = U;
-    if (try_split) {
+    if (R > 0) {
+      // The tail, rank by rank: ranks rt .. N-1, rank r holding cnt(r) tail
+      // units of s_key[r] key tiles each (units of a rank are consecutive).
+      int before = 0;
+      for (int r = lane; r < N; r += 32) before += s_pref[r + 1] <= t0;
+      const int rt = __reduce_add_sync(0xffffffffu, before);
+      auto cnt = [&](int r) { return s_pref[r + 1] - max(s_pref[r], t0); };
       int maxn = 0, minn = 0x7fffffff;
-      for (int i = lane; i < R; i += 32) {
-        maxn = max(maxn, s_key[i]);
-        minn = min(minn, s_key[i]);
+      long long work = 0;
+      for (int r = rt + lane; r < N; r += 32) {
+        const int nk = nkv_of(order_at(r)), cr = cnt(r);
+        s_key[r] = nk;
+        if (cr > 0) {
+          maxn = max(maxn, nk);
+          minn = min(minn, nk);
+          work += (long long)cr * nk;
+        }
       }
+      __syncwarp();
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         maxn = max(maxn, __shfl_xor_sync(0xffffffffu, maxn, o));
         minn = min(minn, __shfl_xor_sync(0xffffffffu, minn, o));
+        work += __shfl_xor_sync(0xffffffffu, work, o);
       }
+      // Items the tail may take.  Equal units in a short tail: one chunk per
+      // CTA, all of about the same length.  Unequal units, or a long tail
+      // (kFineTailTiles key tiles per CTA and more): up to split_cap, so that
+      // the longest-first hand-out of smaller chunks evens out the CTAs'
+      // ends (chunks still hold at least kMinChunkTiles key tiles, enough to
+      // pay for their partial writes and merges).
+      const bool coarse = minn == maxn && work < (long long)kFineTailTiles * p.grid;
+      const int cap = coarse ? p.grid : p.split_cap;
+      auto chunks_of = [&](int nk, int t) { return nk > t ? (nk + t - 1) / t : 1; };
       int lo = 1, hi = maxn > 1 ? maxn : 1;
       if (minn == maxn && maxn > 0) {
         // equal tail units (every single-sequence call): each may take
-        // grid / R chunks, so the smallest budget is ceil(nkv / (grid / R))
-        const int per = p.grid / R;  // >= 1, as R < grid
+        // cap / R chunks, so the smallest budget is ceil(nkv / that)
+        const int per = max(cap / R, 1);
         lo = hi = (maxn + per - 1) / per;
       }
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
         int sum = 0;
-        for (int i = lane; i < R; i += 32) sum += s_key[i] > mid ? (s_key[i] + mid - 1) / mid : 1;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (sum <= p.grid) hi = mid; else lo = mid + 1;
+        for (int r = rt + lane; r < N; r += 32) sum += cnt(r) * chunks_of(s_key[r], mid);
+        sum = __reduce_add_sync(0xffffffffu, sum);
+        if (sum <= cap) hi = mid; else lo = mid + 1;
       }
+      lo = max(lo, kMinChunkTiles);
       if (lo + kMergeTiles < maxn) {
-        // chunk counts -> exclusive prefix (each lane a contiguous block)
+        // chunk counts -> exclusive prefix per tail unit: each lane takes a
+        // contiguous block of ranks, and a rank's units follow one another
         const SplitLayout SL = split_layout(p.split_cap);
         int* tp = reinterpret_cast<int*>(p.split + SL.prefix);
-        const int per = (R + 31) / 32, i0 = lane * per, i1 = min(R, i0 + per);
+        const int per = (N - rt + 31) / 32, r0 = rt + lane * per, r1 = min(N, r0 + per);
         int mine = 0;
-        for (int i = i0; i < i1; ++i) mine += s_key[i] > lo ? (s_key[i] + lo - 1) / lo : 1;
+        for (int r = r0; r < r1; ++r) mine += cnt(r) * chunks_of(s_key[r], lo);
         int incl = mine;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -490,9 +636,10 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
           if (lane >= o) incl += y;
         }
         int run_items = incl - mine;
-        for (int i = i0; i < i1; ++i) {
-          tp[i] = run_items;
-          run_items += s_key[i] > lo ? (s_key[i] + lo - 1) / lo : 1;
+        for (int r = r0; r < r1; ++r) {
+          const int q = chunks_of(s_key[r], lo), f = max(s_pref[r], t0) - t0, cr = cnt(r);
+          for (int j = 0; j < cr; ++j) tp[f + j] = run_items + j * q;
+          run_items += cr * q;
         }
         const int total = __shfl_sync(0xffffffffu, incl, 31);
         if (lane == 0) tp[R] = total;
@@ -505,103 +652,106 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
       hdr[2] = items;
       hdr[3] = split_start;
       hdr[kHdrNextItem] = 0;
-      s_warp[0] = U - split_start;  // tail units whose row counters must be zero
     }
   }
-  __syncthreads();
-  const int nzero = s_warp[0];
-  if (nzero > 0) {
-    // 2 x 128 int counters per tail unit, 16 bytes at a time (the region is
-    // 256-byte aligned)
-    uint4* cnt = reinterpret_cast<uint4*>(p.split + split_layout(p.split_cap).counters);
-    for (int i = tid; i < nzero * 2 * kBlockM / 4; i += nt) cnt[i] = make_uint4(0, 0, 0, 0);
+  // The split region's row counters: every merge leaves its counter at zero,
+  // so they are zeroed only when marked dirty (a new workspace, or a call in
+  // which a CTA gave up a wait), 16 bytes at a time (the region is 256-byte
+  // aligned).
+  if (counters_dirty != 0) {
+    uint4* c4 = reinterpret_cast<uint4*>(p.split + split_layout(p.split_cap).counters);
+    for (int i = tid; i < p.split_cap * 2 * kBlockM / 4; i += nt) c4[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    if (tid == 0) hdr[kHdrCountersDirty] = 0;
   }
 }
 
-// Epilogue of one chunk of a split unit for one row (softmax thread of Q
-// tile t, row r), in two steps.  split_store: the unnormalised O row goes to
-// partial slot `part`.  split_finish: (m, l) go next to it and the chunk is
-// counted in; the last chunk of the unit to finish that row (a counter per
-// row and Q tile) merges the unit's chunks in chunk order,
+// Epilogue of one chunk of a split unit (a softmax warp of Q tile t; lane =
+// row r).  The chunk's unnormalised O row, m and l go to its partial slot,
+// and the chunk is counted in with an acquire-release add on a counter per
+// (row, Q tile).  The last chunk of the unit to finish a row merges,
 //   m* = max_c m_c,  O = sum_c 2^(m_c - m*) O_c,  l = sum_c 2^(m_c - m*) l_c,
-// and writes O / l as bf16.  No thread waits for another CTA.  A slot is
+// always in chunk order (the result does not depend on which chunk came
+// last), and writes O / l as bf16.  Its own chunk is read back from TMEM, so
+// each other chunk costs one batch of loads per pass over the columns (one
+// pass up to 80 columns, two above).  TMEM loads are warp-collective: a warp
+// takes part in the merge if any of its lanes merges.  A slot is
 // column-major ([column][128 rows]) so that a warp's stores and loads of one
-// column are one 128-byte line; partials bypass L1, and the counter's
-// acquire-release add orders them between the chunks.
+// column are one 128-byte line; partials bypass L1.  No thread waits for
+// another CTA.
 constexpr size_t kSlot = (size_t)kPartRowMax * kBlockM;  // floats per (chunk, tile) slot
 
 template <int D>
-__device__ __noinline__ void split_store(uint8_t* parts_base, uint32_t tO, int t, int r, int part) {
+__device__ __noinline__ void split_epilogue(uint8_t* parts_base, int* counters, uint32_t tO, int t,
+                                            int r, float m, float l, uint16_t* orow, bool valid,
+                                            int part, int part0, int tail, int chunks) {
   using G = Geometry<D>;
-  float* mine = reinterpret_cast<float*>(parts_base) + (size_t)(part * 2 + t) * kSlot + r;
-#pragma unroll
-  for (int c = 0; c < G::DP; c += 16) {
-    uint32_t o[16];
-    tmem_ld16(tO + c, o);
-    tmem_wait_ld();
-    reg_fence(o, 0, 16);
-    if (c < D) {
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        if (c + e < D) __stcg(mine + (size_t)(c + e) * kBlockM, __uint_as_float(o[e]));
-    }
-  }
-}
-
-template <int D>
-__device__ __noinline__ void split_finish(uint8_t* parts_base, int* counters, int t, int r,
-                                          float m, float l, uint16_t* orow, bool valid, int part,
-                                          int part0, int tail, int chunks) {
-  using G = Geometry<D>;
+  constexpr int NB = (D + 15) / 16;                 // 16-column TMEM blocks holding O's columns
+  constexpr int PB = D <= 80 ? NB : NB / 2;          // blocks per pass
+  constexpr int PC = D <= 80 ? D : D / 2;            // columns per pass
+  static_assert(D <= 80 || (D % 32 == 0), "two passes of whole 16-column blocks");
   float* parts = reinterpret_cast<float*>(parts_base);
   float* mine = parts + (size_t)(part * 2 + t) * kSlot + r;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    uint32_t o[16];
+    tmem_ld16(tO + 16 * b, o);
+    tmem_wait_ld();
+    reg_fence(o, 0, 16);
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if (16 * b + e < D) __stcg(mine + (size_t)(16 * b + e) * kBlockM, __uint_as_float(o[e]));
+  }
   __stcg(mine + (size_t)G::DP * kBlockM, m);
   __stcg(mine + (size_t)(G::DP + 1) * kBlockM, l);
   int* cnt = counters + ((size_t)(2 * tail + t) * kBlockM + r);
-  if (atom_add_acq_rel_gpu(cnt, 1) != chunks - 1) return;
+  const bool last = atom_add_acq_rel_gpu(cnt, 1) == chunks - 1;
+  if (!__any_sync(0xffffffffu, last)) return;  // warp-uniform from here on
   const float* first = parts + (size_t)(part0 * 2 + t) * kSlot + r;
   const size_t cstride = 2 * kSlot;  // next chunk, same tile and row
+  const int own = part - part0;      // this warp's chunk (the same for all lanes)
   auto mval = [&](int cc) -> float {
-    return cc < chunks ? __ldcg(first + cc * cstride + (size_t)G::DP * kBlockM) : -INFINITY;
-  };
-  auto lval = [&](int cc) -> float {
-    return cc < chunks ? __ldcg(first + cc * cstride + (size_t)(G::DP + 1) * kBlockM) : 0.f;
+    if (cc == own) return m;
+    return last ? __ldcg(first + cc * cstride + (size_t)G::DP * kBlockM) : 0.f;
   };
   float mm = -INFINITY;
-  for (int cc = 0; cc < chunks; cc += 4)
-    mm = fmaxf(fmaxf(mm, fmaxf(mval(cc), mval(cc + 1))), fmaxf(mval(cc + 2), mval(cc + 3)));
+  for (int cc = 0; cc < chunks; ++cc) mm = fmaxf(mm, mval(cc));
   float ll = 0.f;
-  for (int cc = 0; cc < chunks; cc += 4) {
-    float a[4], b[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      a[e] = mval(cc + e);
-      b[e] = lval(cc + e);
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) ll += cc + e < chunks ? ex2(a[e] - mm) * b[e] : 0.f;
+  for (int cc = 0; cc < chunks; ++cc) {
+    const float lc = cc == own ? l : (last ? __ldcg(first + cc * cstride + (size_t)(G::DP + 1) * kBlockM) : 0.f);
+    ll += ex2(mval(cc) - mm) * lc;
   }
-  const float inv_l = 1.0f / ll;
-  // O in blocks of columns; one chunk's block per pass, its loads independent
-  constexpr int BC = D % 32 == 0 ? 32 : (D % 24 == 0 ? 24 : 40);
-  static_assert(D % BC == 0 && BC % 8 == 0, "merge blocks");
+  const float inv_l = ll > 0.f ? 1.0f / ll : 0.f;
 #pragma unroll 1
-  for (int c0 = 0; c0 < D; c0 += BC) {
-    float acc[BC];
+  for (int c0 = 0; c0 < D; c0 += PC) {
+    float acc[PC];
 #pragma unroll
-    for (int e = 0; e < BC; ++e) acc[e] = 0.f;
+    for (int e = 0; e < PC; ++e) acc[e] = 0.f;
     for (int cc = 0; cc < chunks; ++cc) {
-      const float* src = first + cc * cstride + (size_t)c0 * kBlockM;
-      float v[BC];
-#pragma unroll
-      for (int e = 0; e < BC; ++e) v[e] = __ldcg(src + (size_t)e * kBlockM);
       const float w = ex2(mval(cc) - mm);
+      if (cc == own) {
 #pragma unroll
-      for (int e = 0; e < BC; ++e) acc[e] += w * v[e];
+        for (int b = 0; b < PB; ++b) {
+          uint32_t o[16];
+          tmem_ld16(tO + (uint32_t)c0 + 16 * b, o);
+          tmem_wait_ld();
+          reg_fence(o, 0, 16);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (16 * b + e < PC) acc[16 * b + e] += w * __uint_as_float(o[e]);
+        }
+      } else if (last) {
+        const float* src = first + cc * cstride + (size_t)c0 * kBlockM;
+        float v[PC];
+#pragma unroll
+        for (int e = 0; e < PC; ++e) v[e] = __ldcg(src + (size_t)e * kBlockM);
+#pragma unroll
+        for (int e = 0; e < PC; ++e) acc[e] += w * v[e];
+      }
     }
-    if (valid) {
+    if (last && valid) {
 #pragma unroll
-      for (int e = 0; e < BC; e += 8)
+      for (int e = 0; e < PC; e += 8)
         *reinterpret_cast<uint4*>(orow + c0 + e) = make_uint4(
             pack_bf16x2(acc[e] * inv_l, acc[e + 1] * inv_l),
             pack_bf16x2(acc[e + 2] * inv_l, acc[e + 3] * inv_l),
@@ -609,7 +759,7 @@ __device__ __noinline__ void split_finish(uint8_t* parts_base, int* counters, in
             pack_bf16x2(acc[e + 6] * inv_l, acc[e + 7] * inv_l));
     }
   }
-  *cnt = 0;  // ready for the next call
+  if (last) *cnt = 0;  // ready for the next call
 }
 
 // -------------------------------------------------------------------- fwd
@@ -727,11 +877,18 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
       __syncwarp();
       if (leader) mbar_arrive(bar(G::B_ITEM_FULL + islot));
       if (u >= num_items) break;
+#if !ATTN_VARLEN_LATE_CLAIM
       if (leader) pending = atomicAdd(p.status + kHdrNextItem, 1);
+#endif
       const UnitInfo ui = decode_item(u, order, prefix, p.num_seqs, p.cu_q, p.cu_k, G::KN,
                                         split_start, num_units, tail_prefix, p.causal != 0,
                                         p.head_begin);
-      if (ui.nkv == 0) continue;
+      if (ui.nkv == 0) {
+#if ATTN_VARLEN_LATE_CLAIM
+        if (leader) pending = atomicAdd(p.status + kHdrNextItem, 1);
+#endif
+        continue;
+      }
       // maps of this sequence: box A of q, k, v, then box B of q, k, v
       const uint8_t* mq = p.ws + L.maps + (size_t)ui.seq * kMapsPerSeq * kMapBytes;
       const uint8_t* mk = mq + kMapBytes;
@@ -782,6 +939,13 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
                          G::BW, ui.head, row);
         ++kv_item;
       }
+#if ATTN_VARLEN_LATE_CLAIM
+      // the next item is claimed only once this one's last K/V load is out,
+      // a few key tiles before its compute ends: the claim's round trip is
+      // still hidden, and the longest-first order holds (claimed at the start
+      // of an item, a long item's successor was taken one whole item early)
+      if (leader) pending = atomicAdd(p.status + kHdrNextItem, 1);
+#endif
     }
     if (!ok) {
       // let every copy already issued land before the CTA can exit
@@ -1223,9 +1387,8 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
         l = __uint_as_float(o[D % 16]);
       }
       if (ui.part >= 0) {
-        split_store<D>(p.split + SL.parts, tO, t, r, ui.part);
-        split_finish<D>(p.split + SL.parts, reinterpret_cast<int*>(p.split + SL.counters), t, r, m,
-                        l, orow, valid, ui.part, ui.part0, ui.tail, ui.chunks);
+        split_epilogue<D>(p.split + SL.parts, reinterpret_cast<int*>(p.split + SL.counters), tO, t,
+                          r, m, l, orow, valid, ui.part, ui.part0, ui.tail, ui.chunks);
         continue;
       }
       // TMEM -> registers (O / l, bf16) -> shared memory -> TMA store.  Each
@@ -1305,6 +1468,8 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  // a CTA that gave up may have left split-region row counters counted in
+  if (threadIdx.x == 0 && *abort_flag && p.split_cap > 0) p.status[kHdrCountersDirty] = 1;
   if (warp == G::MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
