@@ -517,6 +517,7 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
             // later ranks step by step, one group of CTAs at a time
             for (int r = 1; r < N && found == U && done_all; ++r) {
               const int i = order_at(r), k = units_of(i);
+              if (k == 0) break;  // ranks without units come last
               const unsigned n = (unsigned)(nkv_of(i) + kUnitCostTiles);
               for (int d = 0; d < k;) {
                 if (++steps > kSimMaxSteps) {
@@ -582,7 +583,8 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
       int maxn = 0, minn = 0x7fffffff;
       long long work = 0;
       for (int r = rt + lane; r < N; r += 32) {
-        const int nk = nkv_of(order_at(r)), cr = cnt(r);
+        const int cr = cnt(r);
+        const int nk = cr > 0 ? nkv_of(order_at(r)) : 0;
         s_key[r] = nk;
         if (cr > 0) {
           maxn = max(maxn, nk);
@@ -616,7 +618,10 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
         int sum = 0;
-        for (int r = rt + lane; r < N; r += 32) sum += cnt(r) * chunks_of(s_key[r], mid);
+        for (int r = rt + lane; r < N; r += 32) {
+          const int cr = cnt(r);
+          if (cr > 0) sum += cr * chunks_of(s_key[r], mid);
+        }
         sum = __reduce_add_sync(0xffffffffu, sum);
         if (sum <= cap) hi = mid; else lo = mid + 1;
       }
@@ -628,7 +633,10 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
         int* tp = reinterpret_cast<int*>(p.split + SL.prefix);
         const int per = (N - rt + 31) / 32, r0 = rt + lane * per, r1 = min(N, r0 + per);
         int mine = 0;
-        for (int r = r0; r < r1; ++r) mine += cnt(r) * chunks_of(s_key[r], lo);
+        for (int r = r0; r < r1; ++r) {
+          const int cr = cnt(r);
+          if (cr > 0) mine += cr * chunks_of(s_key[r], lo);
+        }
         int incl = mine;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -637,7 +645,9 @@ __global__ void __launch_bounds__(1024, 1) attn_varlen_plan_kernel(const __grid_
         }
         int run_items = incl - mine;
         for (int r = r0; r < r1; ++r) {
-          const int q = chunks_of(s_key[r], lo), f = max(s_pref[r], t0) - t0, cr = cnt(r);
+          const int cr = cnt(r);
+          if (cr == 0) continue;
+          const int q = chunks_of(s_key[r], lo), f = max(s_pref[r], t0) - t0;
           for (int j = 0; j < cr; ++j) tp[f + j] = run_items + j * q;
           run_items += cr * q;
         }
