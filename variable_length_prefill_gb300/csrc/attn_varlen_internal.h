@@ -41,9 +41,9 @@ constexpr int kHdrCountersDirty = 5;
 // Workspace: [header 256 B][tensor maps][order int32 N][prefix int32 N+1]
 //   header: int32 status, num_units, num_items, split_start, next_item,
 //           counters_dirty
-// Work items: items [0, split_start) are whole units; the units of the last,
-// partial wave, [split_start, num_units), may be split along the key range
-// into several items each (see SplitLayout).
+// Work items: items [0, split_start) are whole units; the tail units the plan
+// kernel found late in the schedule, [split_start, num_units), may be split
+// along the key range into several items each (see SplitLayout).
 struct WsLayout {
   size_t maps;
   size_t order;

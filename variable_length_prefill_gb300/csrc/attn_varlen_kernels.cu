@@ -10,21 +10,24 @@
 //  1. plan (one CTA): reads cu_seqlens on the device, counts the work units
 //     of every sequence (a unit is one head x 256 query rows), orders the
 //     sequences longest-key-range first, writes the prefix sums of the units
-//     in that order, and writes one q, one k and one v tensor map per
-//     sequence by patching host-encoded templates (global address = the
-//     sequence's first row, row extent = the sequence length) so that TMA
-//     zero-fills every row past the end of a sequence.  The template is
-//     chosen by the sequence's byte size (see kMapLargeBytes), which makes
-//     each patched map identical to the one the host encoder would produce.
+//     in that order, and writes the q, k, v and out tensor maps of every
+//     sequence (box A and box B) by patching host-encoded templates (global
+//     address = the sequence's first row, row extent = the sequence length)
+//     so that TMA zero-fills every row past the end of a sequence and clips
+//     stores there.  The template is chosen by the sequence's byte size (see
+//     kMapLargeBytes), which makes each patched map identical to the one the
+//     host encoder would produce.  It then plans the key-range split of the
+//     units at the end of the schedule (step 4 of the kernel).
 //
-//  2. fwd (persistent, one CTA per SM): each CTA walks the unit list with a
-//     stride of gridDim.x.  Warp roles:
+//  2. fwd (persistent, one CTA per SM): the first item of a CTA is its
+//     blockIdx.x, later ones come from a workspace counter, whole units in
+//     longest-first order and then the split units' chunks.  Warp roles:
 //       warps 0-3  softmax for Q tile 0 (TMEM lanes 0-127 = its 128 rows)
 //       warps 4-7  softmax for Q tile 1
 //       warp  8    TMA producer: Q tiles, then a ring of K and V tiles
 //       warp  9    TMEM owner and tcgen05.mma issuer (head_dim 128: both
-//                  tiles; head_dim 72: tile 0)
-//       warp 10    head_dim 72 only: tcgen05.mma issuer for tile 1
+//                  tiles; head_dim 64-96: tile 0)
+//       warp 10    head_dim 64-96 only: tcgen05.mma issuer for tile 1
 //     Softmax is an online exp2 softmax, one row per thread, with a lazy
 //     rescale: the running max is only raised (and O rescaled in TMEM) when a
 //     row's new max exceeds it by more than kRescaleThreshold (log2 units).
@@ -45,12 +48,14 @@
 //     tile has its own issuer, so neither tile's S waits in one in-order
 //     program behind the other tile's P.V.
 //
-// Head dims: 128 runs natively; 72 is padded to 80.  Both load every tile as
-// two 64-column TMA boxes with 128-byte swizzle; for 72 the second box holds
-// columns 64-71 and TMA zero fill, so columns 72-79 of Q and K add nothing to
-// Q.K^T, the MMAs use K = 80 and N = 80 (the first 16 columns of the second
-// box), and the padded output columns are never stored.  The scale always
-// uses the true head_dim.
+// Head dims 64, 72, 80, 96 and 128 run here (256 has a kernel of its own).
+// Box A holds columns 0-63 with 128-byte swizzle.  For 72, box B is an
+// unswizzled 8-column box (columns 64-71); a zero region in shared memory
+// supplies columns 72-79 of Q and K to the K = 80 MMA step, and a ones region
+// makes V's padding column 72 read 1.0, so P.V also sums each row of P.  For
+// 80, 96 and 128 box B is a second 64-column swizzled box (zero-filled past
+// head_dim).  Padded output columns are never stored.  The scale always uses
+// the true head_dim.
 //
 // Every mbarrier wait is bounded in time; a wait that runs out records a bit
 // in the workspace status word, raises a CTA-wide abort flag, and the CTA
@@ -874,8 +879,8 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
     // Items are handed out dynamically, longest first: the CTA's first item
     // is blockIdx.x, every later one comes from the workspace counter.  The
     // producer publishes each item (or a past-the-end index) in the ring.
-    // The counter is read one item ahead, so its round trip overlaps the
-    // current item's loads.
+    // The next item is claimed once the current item's last K/V load is out,
+    // so the counter's round trip overlaps that item's last key tiles.
     const int leader_lane = __ffs(__ballot_sync(0xffffffffu, leader != 0)) - 1;
     int pending = 0;
     for (int k = 0; ok; ++k) {
@@ -1487,9 +1492,10 @@ __global__ void __launch_bounds__(Geometry<D>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------- launch
-// A small batch plans in four warps or eight (fewer threads to launch and to
-// synchronise; four warps still spread the map writes and the zeroing of the
-// tail split's counters); the kernel's loops take any multiple of 32 threads.
+// A small batch plans in four warps, a larger one in eight or 32 (fewer
+// threads to launch and to synchronise; four warps still spread the map
+// writes and, when they are dirty, the zeroing of the split region's row
+// counters); the kernel's loops take any multiple of 32 threads.
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
   const int threads = p.num_seqs <= 128 ? 128 : (p.num_seqs <= 256 ? 256 : 1024);
 #if ATTN_VARLEN_PLAN_PDL
